@@ -1,0 +1,238 @@
+/*
+ * lsx.h -- C ABI of liblsx: exact softmax attention computed blockwise over
+ * sequence chunks, on one NVIDIA GB300 (sm_103a).
+ *
+ * The method (sources are the pages' titles and sections):
+ *  - BurstAttention: An Efficient Distributed Attention Framework for
+ *    Extremely Long Sequences -- method section: the sequence is split into
+ *    chunks; each device computes "local attention" of its query chunk against
+ *    key/value chunks and the local results are aggregated into global ones.
+ *  - Lean Attention (abstract): the associative property of online softmax
+ *    makes the combination of partial results a reduction.
+ *  - Tree Attention: Topology-aware Decoding for Long-Context Attention on GPU
+ *    clusters (abstract): the reduction across the sequence axis is computed
+ *    as a tree reduction.
+ *  - DistFlashAttn ("Effiziente verteilte Aufmerksamkeit ...", core concepts):
+ *    load-balanced scheduling of causal work across workers, and a backward
+ *    pass that reuses the saved attention output instead of re-running the
+ *    forward pass.
+ *
+ * Conventions shared by every entry point
+ *  - Tensors are rank-4 views [B, H, N, D] described by lsx_tensor.  The D
+ *    axis is contiguous (stride 1); the other strides are in ELEMENTS.  A
+ *    log-sum-exp tensor is a view with D == 1 (its stride_n must be 1).
+ *  - Every buffer is owned by the caller.  The library allocates no device or
+ *    host memory; scratch space ("workspace") is passed in by the caller, who
+ *    sizes it with the matching *_workspace_size call.  A workspace may be
+ *    reused by the next call once that call's stream has reached it.
+ *  - Pointers are DEVICE pointers unless an entry point says otherwise.
+ *    Device data must be 16-byte aligned; for bf16 tensors fed to the tensor
+ *    core path, every stride must also be a multiple of 8 elements.
+ *  - Every call is enqueued on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns without synchronising.
+ *  - Return value: LSX_OK, or a negative LSX_ERR_* code.  A call that returns
+ *    an error has launched nothing and touched no buffer.  A failure detected
+ *    on the device (a bounded wait that ran out) is recorded in a per-device
+ *    status word that lsx_sync_status reads back.
+ *  - Softmax scale: scores are scale * <q_i, k_j>; scale <= 0 selects
+ *    1/sqrt(D).  LSE is in natural-log units of the scaled scores.
+ *  - Causal masking uses ABSOLUTE positions: query row i of a chunk that
+ *    starts at q_off sees key row j of a chunk that starts at kv_off iff
+ *    kv_off + j <= q_off + i.  A query with no visible key gets O = 0 and
+ *    LSE = -inf, the identity of the merge.
+ *  - Grouped query heads: query head h reads key/value head h / (Hq / Hkv).
+ */
+#ifndef LSX_H
+#define LSX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* lsx_stream_t; /* identical to cudaStream_t */
+
+enum lsx_dtype { LSX_BF16 = 0, LSX_F32 = 1 };
+
+enum lsx_status {
+  LSX_OK = 0,
+  LSX_ERR_NULL = -1,        /* a required pointer is NULL                    */
+  LSX_ERR_SHAPE = -2,       /* shapes disagree                               */
+  LSX_ERR_DTYPE = -3,       /* dtype combination not supported               */
+  LSX_ERR_ALIGN = -4,       /* base or stride alignment violated             */
+  LSX_ERR_UNSUPPORTED = -5, /* valid request outside what is implemented     */
+  LSX_ERR_WORKSPACE = -6,   /* workspace missing or too small                */
+  LSX_ERR_LAUNCH = -7,      /* a CUDA launch or API call failed              */
+  LSX_ERR_TIMEOUT = -8,     /* a device-side bounded wait ran out            */
+  LSX_ERR_DEVICE = -9       /* no usable sm_103 device / context             */
+};
+
+typedef struct lsx_tensor {
+  void* data;      /* base pointer (device unless stated otherwise)          */
+  int32_t dtype;   /* enum lsx_dtype                                         */
+  int32_t reserved;
+  int64_t B, H, N, D;
+  int64_t stride_b, stride_h, stride_n; /* elements; stride of D is 1        */
+} lsx_tensor;
+
+/* ------------------------------------------------------------------------
+ * attn_chunk_fwd -- local attention of one (query chunk, key/value chunk)
+ * pair (BurstAttention, method: local attention computation; Lean Attention,
+ * abstract: online softmax).
+ *   q  [B, Hq, Lq, D]    bf16 or f32
+ *   k  [B, Hkv, Lk, D]   same dtype as q
+ *   v  [B, Hkv, Lk, D]   same dtype as q
+ *   o  [B, Hq, Lq, D]    out: bf16 or f32 (f32 inputs need f32 o)
+ *   lse[B, Hq, Lq, 1]    out: f32, natural log
+ * accumulate == 0: o, lse receive this pair's normalised partial.
+ * accumulate == 1: o, lse hold a partial over other keys; the new partial is
+ *   merged into them in the epilogue (the LSE-weighted merge of attn_merge).
+ * D in {64, 128}.  bf16 inputs run on the tcgen05 tensor cores (fp32
+ * accumulation, P rounded to bf16 for the P.V product); f32 inputs run an
+ * fp32 CUDA-core path.  No workspace is used (workspace may be NULL).
+ * ---------------------------------------------------------------------- */
+int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
+                   const lsx_tensor* v, int64_t q_off, int64_t kv_off,
+                   int causal, float scale, const lsx_tensor* o,
+                   const lsx_tensor* lse, int accumulate, void* workspace,
+                   size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_merge -- LSE-weighted merge of two partials over disjoint key sets
+ * (BurstAttention abstract: aggregate local results into global ones;
+ * Lean Attention abstract: the merge is associative):
+ *   LSE = m + log(exp(LSE_a - m) + exp(LSE_b - m)),  m = max(LSE_a, LSE_b)
+ *   O   = exp(LSE_a - LSE) O_a + exp(LSE_b - LSE) O_b
+ * o_a, o_b, o_out: [B, H, N, D] bf16 or f32 (each independently);
+ * lse_*: [B, H, N, 1] f32.  o_out/lse_out may alias o_a/lse_a or o_b/lse_b
+ * exactly (same base and strides).  Two -inf inputs give O = 0, LSE = -inf.
+ * D in {64, 128}.
+ * ---------------------------------------------------------------------- */
+int attn_merge(const lsx_tensor* o_a, const lsx_tensor* lse_a,
+               const lsx_tensor* o_b, const lsx_tensor* lse_b,
+               const lsx_tensor* o_out, const lsx_tensor* lse_out,
+               lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_tree_merge -- one-pass reduction of n_parts partials (Tree Attention
+ * abstract: tree reduction across the sequence axis; DeFT abstract: global
+ * reduction of partial attention).  Partial p of every row is combined in a
+ * fixed order, so the result is bit-deterministic.
+ *   o_parts:   [B, H, N, D] view of partial 0; partial p starts at
+ *              data + p * part_stride_o elements (bf16 or f32)
+ *   lse_parts: [B, H, N, 1] view of partial 0; partial p starts at
+ *              data + p * part_stride_lse elements (f32)
+ *   o_out [B, H, N, D] bf16 or f32; lse_out [B, H, N, 1] f32 (may be NULL
+ *   data to skip writing LSE).
+ * 1 <= n_parts <= 4096.  D in {64, 128}.
+ * ---------------------------------------------------------------------- */
+int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
+                    const lsx_tensor* lse_parts, int64_t part_stride_lse,
+                    int n_parts, const lsx_tensor* o_out,
+                    const lsx_tensor* lse_out, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_chunk_bwd -- gradients of one chunk pair from the SAVED final output
+ * and log-sum-exp, without re-running the forward pass (DistFlashAttn, core
+ * concepts: rematerialization-aware gradient checkpointing).
+ *   q, k, v as in attn_chunk_fwd; o [B,Hq,Lq,D] and lse [B,Hq,Lq,1] are the
+ *   FINAL (fully merged) output and LSE of the query rows; d_o like o.
+ *   dq [B,Hq,Lq,D], dk/dv [B,Hkv,Lk,D]: out, bf16 or f32.
+ * accumulate == 0: outputs receive this pair's contribution.
+ * accumulate == 1: the contribution is added to the outputs (use f32
+ *   outputs to sum over many chunk pairs).
+ * Workspace: attn_chunk_bwd_workspace_size bytes (row sums D_i = <dO_i,O_i>).
+ * ---------------------------------------------------------------------- */
+size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
+int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
+                   const lsx_tensor* v, const lsx_tensor* o,
+                   const lsx_tensor* lse, const lsx_tensor* d_o,
+                   int64_t q_off, int64_t kv_off, int causal, float scale,
+                   const lsx_tensor* dq, const lsx_tensor* dk,
+                   const lsx_tensor* dv, int accumulate, void* workspace,
+                   size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_chunked_fwd / attn_chunked_bwd -- a whole sequence [B, H, N, D] split
+ * into chunks of chunk_len rows, every (query chunk, key chunk) pair that the
+ * mask leaves visible computed in ONE persistent launch whose CTAs take
+ * work items from a longest-first causal schedule (DistFlashAttn, core
+ * concepts: load-balanced scheduling; here the workers are the SMs).  Query
+ * rows whose key range is long may be split into pieces whose partials are
+ * combined by the tree merge (Lean Attention abstract: stream-K style
+ * reduction); workspace then holds those partials.
+ * chunk_len must be a multiple of 128.  Same dtypes as the chunk calls.
+ * ---------------------------------------------------------------------- */
+size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
+                                       int64_t chunk_len, int causal);
+int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
+                     const lsx_tensor* v, int64_t chunk_len, int causal,
+                     float scale, const lsx_tensor* o, const lsx_tensor* lse,
+                     void* workspace, size_t workspace_bytes,
+                     lsx_stream_t stream);
+size_t attn_chunked_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
+                                       int64_t chunk_len, int causal);
+int attn_chunked_bwd(const lsx_tensor* q, const lsx_tensor* k,
+                     const lsx_tensor* v, const lsx_tensor* o,
+                     const lsx_tensor* lse, const lsx_tensor* d_o,
+                     int64_t chunk_len, int causal, float scale,
+                     const lsx_tensor* dq, const lsx_tensor* dk,
+                     const lsx_tensor* dv, void* workspace,
+                     size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * attn_decode -- one query token per sequence against a long key/value
+ * cache split into chunks of chunk_len keys; each chunk yields a partial
+ * (O, LSE) and the partials are tree-reduced (Tree Attention abstract;
+ * Lean Attention abstract: split-KV decode with a parallel reduction).
+ *   q [B, Hq, 1, D] bf16; kc, vc [B, Hkv, N, D] bf16 (Hq / Hkv in
+ *   {1, 2, 4, 8}); o [B, Hq, 1, D] bf16 or f32; lse [B, Hq, 1, 1] f32.
+ * The query sees every key (no mask).  D == 128.
+ * Workspace: attn_decode_workspace_size bytes (the per-chunk partials).
+ * ---------------------------------------------------------------------- */
+size_t attn_decode_workspace_size(const lsx_tensor* q, const lsx_tensor* kc,
+                                  int64_t chunk_len);
+int attn_decode(const lsx_tensor* q, const lsx_tensor* kc,
+                const lsx_tensor* vc, int64_t chunk_len, float scale,
+                const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Status, diagnostics and host-side helpers.
+ * ---------------------------------------------------------------------- */
+
+/* Synchronises `stream`, returns the current device's status word (LSX_OK or
+ * e.g. LSX_ERR_TIMEOUT) and clears it. */
+int lsx_sync_status(lsx_stream_t stream);
+
+/* Static string for a status code (never NULL). */
+const char* lsx_status_string(int code);
+
+/* Upper bound, in nanoseconds, of every device-side wait on an mbarrier
+ * before the kernel gives up, records LSX_ERR_TIMEOUT and exits.  0 restores
+ * the default (10 s).  Process-wide; affects launches made after the call. */
+void lsx_set_wait_limit_ns(uint64_t ns);
+
+/* Launches one block that waits on an mbarrier nothing will ever complete,
+ * under the current wait limit, so that callers can check that a bounded wait
+ * ends and reports LSX_ERR_TIMEOUT through lsx_sync_status (no fault, no
+ * hang). */
+int lsx_selftest_bounded_wait(lsx_stream_t stream);
+
+/* Host-only: simulate the forward work schedule that attn_chunked_fwd would
+ * use for [B, H, N] with chunk_len and causal, on n_workers persistent
+ * workers, with each work item costed by its visible key tiles.  Writes
+ * makespan (max tiles on one worker), the ideal (total / n_workers, rounded
+ * up) and the total into out[0..2].  host pointers. */
+int lsx_schedule_stats(int64_t B, int64_t H, int64_t N, int64_t chunk_len,
+                       int causal, int n_workers, int64_t* out);
+
+/* Library version string, e.g. "lsx 0.1 sm_103a". */
+const char* lsx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LSX_H */

@@ -1,0 +1,30 @@
+"""Exact softmax attention computed blockwise over sequence chunks on one GB300.
+
+The compute lives in ``liblsx.so`` (hand-written CUDA for sm_103a, C ABI in
+``include/lsx.h``); ``attention`` is a thin ctypes binding with the same
+entry points.  Importing this package does not load the library; the first
+call does, and raises if it has not been built.
+"""
+
+from .attention import (  # noqa: F401
+    chunk_bwd,
+    chunk_fwd,
+    chunked_bwd,
+    chunked_fwd,
+    decode,
+    decode_workspace_size,
+    merge,
+    schedule_stats,
+    selftest_bounded_wait,
+    set_wait_limit_ns,
+    status_string,
+    sync_status,
+    tree_merge,
+    version,
+)
+
+__all__ = [
+    "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "merge", "tree_merge",
+    "decode", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
+    "set_wait_limit_ns", "status_string", "sync_status", "version",
+]

@@ -1,0 +1,514 @@
+// fwd_tc.cu -- tcgen05 forward of exact attention over chunk pairs (bf16 in,
+// fp32 accumulation in tensor memory).
+//
+// What it computes: for every query row i of a query chunk (absolute start
+// q_off) against a key/value chunk (absolute start kv_off), the normalised
+// output O_i = softmax(scale * q_i K^T) V over the visible keys and
+// LSE_i = log sum_j exp(scale * <q_i, k_j>).  This is the "local attention
+// computation" of BurstAttention (method section), evaluated with the online
+// softmax whose associativity Lean Attention (abstract) relies on: a running
+// row maximum m and sum l, with the output rescaled whenever m grows.
+//
+// Work decomposition (DistFlashAttn core concepts, load-balanced scheduling,
+// with SMs as the workers): a persistent grid of one CTA per SM; a work item
+// is two adjacent 128-row query tiles of one (batch, head); items are dealt
+// longest-first in snake order.  Within an item the CTA walks every visible
+// 128-key tile in order; crossing a key-chunk boundary simply continues the
+// online softmax, which equals computing each chunk pair's partial and
+// merging the partials in that order.
+//
+// CTA roles (384 threads):
+//   warp 0        TMA producer: Q tiles once per item, K/V tiles through a
+//                 ring of kStages stages (128-byte swizzle, zero fill past
+//                 the end of a chunk).
+//   warp 1        TMEM owner; lane 0 issues every tcgen05.mma:
+//                 S_t = Q_t K^T   (SS, both K-major)            -> TMEM S_t
+//                 O_t += P_t V    (TS, P_t from TMEM, V MN-major) -> TMEM O_t
+//   warps 4..7    softmax of query tile 0 (thread = row = TMEM lane)
+//   warps 8..11   softmax of query tile 1
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [384,384+D);
+// P_t (bf16 pairs) overwrites the first 64 columns of S_t after the softmax
+// has read S_t, and S_t is only re-issued once the P_t V product completed.
+// The two query tiles ping-pong: the tensor pipe computes one tile's
+// products while the other tile's softmax runs on the CUDA cores.
+//
+// Rescaling: the output is rescaled only when the row maximum grows by more
+// than 8 (base 2); otherwise the stale maximum is kept, so exp2 arguments
+// stay <= 8 (P <= 256), and the final O / l uses one consistent maximum, so
+// the result is unchanged.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace lsx {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row bf16 tile
+  static constexpr int kSub = D / 64;             // 64-column (128 B) boxes
+};
+
+template <int D>
+struct __align__(1024) FwdSmem {
+  __nv_bfloat16 q[2][128 * D];
+  __nv_bfloat16 k[FwdCfg<D>::kStages][128 * D];
+  __nv_bfloat16 v[FwdCfg<D>::kStages][128 * D];
+  uint64_t q_full, q_empty, final_bar;
+  uint64_t k_full[FwdCfg<D>::kStages];
+  uint64_t v_full[FwdCfg<D>::kStages];
+  uint64_t kv_empty[FwdCfg<D>::kStages];
+  uint64_t s_full[2], p_full[2], o_full[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+struct FwdParams {
+  int64_t B, Hq, Hkv, Lq, Lk;
+  int64_t q_off, kv_off;
+  int causal, accumulate;
+  float scale_log2;
+  int64_t n_qpairs, n_items;
+  void* o;
+  int o_f32;
+  int64_t o_sb, o_sh, o_sn;
+  float* lse;
+  int64_t l_sb, l_sh, l_sn;
+  int* status;
+  uint64_t wait_ns;
+};
+
+struct Item {
+  int64_t b, h, hk, pair;
+  int64_t nkv[2];
+};
+
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
+  Item x;
+  const int64_t bh_n = p.B * p.Hq;
+  x.pair = p.n_qpairs - 1 - it / bh_n;
+  const int64_t bh = it % bh_n;
+  x.b = bh / p.Hq;
+  x.h = bh % p.Hq;
+  x.hk = x.h / (p.Hq / p.Hkv);
+  for (int t = 0; t < 2; ++t)
+    x.nkv[t] = fwd_kv_tiles(2 * x.pair + t, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal);
+  return x;
+}
+
+// Wait that ignores the abort flag but keeps the time bound (used at exit).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
+                                           uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > limit_ns) break;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v,
+                  const FwdParams p) {
+  using Cfg = FwdCfg<D>;
+  constexpr int kStages = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem<D>& sm = *reinterpret_cast<FwdSmem<D>*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const WaitGuard guard{p.status, p.wait_ns, &sm.abort};
+
+  if (threadIdx.x == 0) {
+    sm.abort = 0;
+    mbar_init(&sm.q_full, 1);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.final_bar, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.k_full[s], 1);
+      mbar_init(&sm.v_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&sm.s_full[t], 1);
+      mbar_init(&sm.p_full[t], 128);
+      mbar_init(&sm.o_full[t], 1);
+    }
+    fence_barrier_init();
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_v);
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  const int64_t G = gridDim.x;
+  const int64_t c = blockIdx.x;
+  // 384 threads launched at <= 168 registers (64,512).  Producer/MMA
+  // warpgroup keeps 64, the two softmax warpgroups take 216:
+  // 128 * 64 + 256 * 216 = 63,488 <= 64,512.
+  if (warp < 4) {
+  regs_dec<64>();
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t stage = 0, phase = 0, qe_phase = 0;
+    for (int64_t r = 0;; ++r) {
+      const int64_t it = snake_item(c, r, G);
+      if (it >= p.n_items) break;
+      const Item x = decode_item(p, it);
+      const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
+      if (!mbar_wait(&sm.q_empty, qe_phase ^ 1, guard)) break;
+      qe_phase ^= 1;
+      mbar_arrive_expect_tx(&sm.q_full, 2 * Cfg::kTileBytes);
+      for (int t = 0; t < 2; ++t)
+        for (int sub = 0; sub < Cfg::kSub; ++sub)
+          tma_load_4d(&sm.q[t][sub * 128 * 64], &tm_q, &sm.q_full, sub * 64,
+                      static_cast<int>((2 * x.pair + t) * 128),
+                      static_cast<int>(x.h), static_cast<int>(x.b));
+      bool ok = true;
+      for (int64_t j = 0; j < nkv; ++j) {
+        if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
+        mbar_arrive_expect_tx(&sm.k_full[stage], Cfg::kTileBytes);
+        for (int sub = 0; sub < Cfg::kSub; ++sub)
+          tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.k_full[stage],
+                      sub * 64, static_cast<int>(j * 128),
+                      static_cast<int>(x.hk), static_cast<int>(x.b));
+        mbar_arrive_expect_tx(&sm.v_full[stage], Cfg::kTileBytes);
+        for (int sub = 0; sub < Cfg::kSub; ++sub)
+          tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.v_full[stage],
+                      sub * 64, static_cast<int>(j * 128),
+                      static_cast<int>(x.hk), static_cast<int>(x.b));
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------- MMA issuer
+    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, 0, 1);
+    uint32_t stage = 0, phase = 0, q_phase = 0;
+    uint32_t p_phase[2] = {0, 0}, o_phase[2] = {0, 0};
+    bool o_pending[2] = {false, false};
+    bool issued = false;
+    const uint32_t q_addr[2] = {smem_addr(sm.q[0]), smem_addr(sm.q[1])};
+    for (int64_t r = 0;; ++r) {
+      const int64_t it = snake_item(c, r, G);
+      if (it >= p.n_items) break;
+      const Item x = decode_item(p, it);
+      const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
+      if (!mbar_wait(&sm.q_full, q_phase, guard)) break;
+      q_phase ^= 1;
+      tc_fence_after();
+      bool ok = true;
+      for (int64_t j = 0; j < nkv && ok; ++j) {
+        if (!mbar_wait(&sm.k_full[stage], phase, guard)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t k_addr = smem_addr(sm.k[stage]);
+        for (int t = 0; t < 2; ++t) {
+          if (j >= x.nkv[t]) continue;
+          if (o_pending[t]) {  // P_t aliases S_t: wait for the last P_t V
+            if (!mbar_wait(&sm.o_full[t], o_phase[t], guard)) { ok = false; break; }
+            o_phase[t] ^= 1;
+            o_pending[t] = false;
+            tc_fence_after();
+          }
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tmem + t * 128, sdesc_sw128(q_addr[t] + off, 16, 1024),
+                   sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+          }
+          mma_commit(&sm.s_full[t]);
+          issued = true;
+        }
+        if (!ok) break;
+        if (!mbar_wait(&sm.v_full[stage], phase, guard)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_addr(sm.v[stage]);
+        for (int t = 0; t < 2; ++t) {
+          if (j >= x.nkv[t]) continue;
+          if (!mbar_wait(&sm.p_full[t], p_phase[t], guard)) { ok = false; break; }
+          p_phase[t] ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                   sdesc_sw128(v_addr + kk * 2048, 128 * 128, 1024), kIdO,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.o_full[t]);
+          o_pending[t] = true;
+        }
+        if (!ok) break;
+        mma_commit(&sm.kv_empty[stage]);
+        if (++stage == kStages) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      mma_commit(&sm.q_empty);
+    }
+    if (issued) {  // every issued MMA has completed before TMEM is released
+      mma_commit(&sm.final_bar);
+      drain_wait(&sm.final_bar, 0, p.wait_ns);
+    }
+  }
+  } else {
+    regs_inc<216>();
+    // ------------------------------------------------------------- softmax
+    const int t = (warp - 4) >> 2;
+    const int row = threadIdx.x - 128 * (1 + t);  // 0..127 == TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + lane_base + t * 128;
+    const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    uint32_t s_phase = 0;
+    uint32_t pv_count = 0;
+    const float sl2 = p.scale_log2;
+    for (int64_t r = 0;; ++r) {
+      const int64_t it = snake_item(c, r, G);
+      if (it >= p.n_items) break;
+      const Item x = decode_item(p, it);
+      const int64_t nkv = x.nkv[t];
+      const int64_t qr0 = (2 * x.pair + t) * 128;
+      float m = kNegInf, l = 0.f;
+      bool ok = true;
+      for (int64_t j = 0; j < nkv; ++j) {
+        if (!mbar_wait(&sm.s_full[t], s_phase, guard)) { ok = false; break; }
+        s_phase ^= 1;
+        tc_fence_after();
+        float s[128];
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tS + cc * 32, u);
+          tmem_ld_wait32(u);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
+        }
+        const int64_t kb = j * 128;
+        const bool need_mask =
+            (kb + 128 > p.Lk) || (p.causal && p.kv_off + kb + 127 > p.q_off + qr0);
+        if (need_mask) {
+          int64_t lim = 127;
+          if (kb + 128 > p.Lk) lim = p.Lk - kb - 1;
+          if (p.causal) {
+            const int64_t c2 = p.q_off + qr0 + row - p.kv_off - kb;
+            if (c2 < lim) lim = c2;
+          }
+          const int climit = lim < -1 ? -1 : static_cast<int>(lim);
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (i > climit) s[i] = kNegInf;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int i = 4; i < 128; i += 4) {
+          mx0 = fmaxf(mx0, s[i]);
+          mx1 = fmaxf(mx1, s[i + 1]);
+          mx2 = fmaxf(mx2, s[i + 2]);
+          mx3 = fmaxf(mx3, s[i + 3]);
+        }
+        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const float m_new = fmaxf(m, mx * sl2);
+        if (j == 0) {
+          m = m_new;
+        } else {
+          const bool need = m_new > m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            // O_t must hold the finished P_t V of the previous key tile
+            if (!mbar_wait(&sm.o_full[t], (pv_count - 1) & 1, guard)) { ok = false; break; }
+            tc_fence_after();
+            const float alpha = (m == kNegInf) ? 0.f : ex2(m - m_new);
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t u[32];
+              tmem_ld32(tO + cc * 32, u);
+              tmem_ld_wait32(u);
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+              tmem_st32(tO + cc * 32, u);
+            }
+            tmem_st_wait();
+            l *= alpha;
+            m = m_new;
+          }
+        }
+        const float mu = (m == kNegInf) ? 0.f : m;
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a = ex2(fmaf(s[cc * 32 + 2 * i], sl2, -mu));
+            const float b2 = ex2(fmaf(s[cc * 32 + 2 * i + 1], sl2, -mu));
+            l0 += a;
+            l1 += b2;
+            pk[i] = pack_bf16(a, b2);
+          }
+          tmem_st16(tS + cc * 16, pk);
+        }
+        l += l0 + l1;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full[t]);
+        ++pv_count;
+      }
+      if (!ok) break;
+      // --------------------------------------------------------- epilogue
+      const int64_t qrow = qr0 + row;
+      const bool valid = qrow < p.Lq;
+      if (nkv > 0) {
+        if (!mbar_wait(&sm.o_full[t], (pv_count - 1) & 1, guard)) break;
+        tc_fence_after();
+      }
+      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+      float lse_new = (l > 0.f) ? (m + lg2(l)) * kLn2 : kNegInf;
+      float w_old = 0.f, w_new = 1.f;
+      if (p.accumulate && valid) {
+        const float lse_old = p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn];
+        const float mm = fmaxf(lse_old, lse_new);
+        if (mm == kNegInf) {
+          w_old = 0.f; w_new = 0.f;
+        } else {
+          const float wa = expf(lse_old - mm), wb = expf(lse_new - mm);
+          const float tot = wa + wb;
+          w_old = wa / tot; w_new = wb / tot;
+          lse_new = mm + logf(tot);
+        }
+      }
+#pragma unroll
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (nkv > 0) {
+          tmem_ld32(tO + cc * 32, u);
+          tmem_ld_wait32(u);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = 0u;
+        }
+        if (!valid) continue;
+        float ov[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(u[i]) * inv * w_new;
+        const int64_t base = x.b * p.o_sb + x.h * p.o_sh + qrow * p.o_sn + cc * 32;
+        if (p.o_f32) {
+          float* dst = static_cast<float*>(p.o) + base;
+          if (p.accumulate) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              const float4 old = *reinterpret_cast<const float4*>(dst + i);
+              ov[i] += w_old * old.x; ov[i + 1] += w_old * old.y;
+              ov[i + 2] += w_old * old.z; ov[i + 3] += w_old * old.w;
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + i) =
+                make_float4(ov[i], ov[i + 1], ov[i + 2], ov[i + 3]);
+        } else {
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.o) + base;
+          if (p.accumulate) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 8) {
+              const uint4 old = *reinterpret_cast<const uint4*>(dst + i);
+              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&ow[e]);
+                ov[i + 2 * e] += w_old * __low2float(pr);
+                ov[i + 2 * e + 1] += w_old * __high2float(pr);
+              }
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16(ov[i], ov[i + 1]);
+            w.y = pack_bf16(ov[i + 2], ov[i + 3]);
+            w.z = pack_bf16(ov[i + 4], ov[i + 5]);
+            w.w = pack_bf16(ov[i + 6], ov[i + 7]);
+            *reinterpret_cast<uint4*>(dst + i) = w;
+          }
+        }
+      }
+      if (valid) p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn] = lse_new;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
+                    const lsx_tensor& v, int64_t q_off, int64_t kv_off,
+                    int causal, float scale, const lsx_tensor& o,
+                    const lsx_tensor& lse, int accumulate,
+                    const DeviceCtx& ctx, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!make_map_bf16_4d(&tq, q.data, q.B, q.H, q.N, q.D, q.stride_b, q.stride_h,
+                        q.stride_n, 128) ||
+      !make_map_bf16_4d(&tk, k.data, k.B, k.H, k.N, k.D, k.stride_b, k.stride_h,
+                        k.stride_n, 128) ||
+      !make_map_bf16_4d(&tv, v.data, v.B, v.H, v.N, v.D, v.stride_b, v.stride_h,
+                        v.stride_n, 128))
+    return LSX_ERR_LAUNCH;
+  FwdParams p;
+  p.B = q.B; p.Hq = q.H; p.Hkv = k.H; p.Lq = q.N; p.Lk = k.N;
+  p.q_off = q_off; p.kv_off = kv_off;
+  p.causal = causal; p.accumulate = accumulate;
+  p.scale_log2 = scale * kLog2e;
+  p.n_qpairs = ceil_div(q.N, 256);
+  p.n_items = p.n_qpairs * q.B * q.H;
+  p.o = o.data; p.o_f32 = (o.dtype == LSX_F32);
+  p.o_sb = o.stride_b; p.o_sh = o.stride_h; p.o_sn = o.stride_n;
+  p.lse = static_cast<float*>(lse.data);
+  p.l_sb = lse.stride_b; p.l_sh = lse.stride_h; p.l_sn = lse.stride_n;
+  p.status = ctx.status; p.wait_ns = ctx.wait_ns;
+  const size_t smem = sizeof(FwdSmem<D>) + 1024;
+  if (cudaFuncSetAttribute(fwd_tc_kernel<D>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return LSX_ERR_LAUNCH;
+  const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+  fwd_tc_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, p);
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+}  // namespace
+
+int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
+                  const lsx_tensor& v, int64_t q_off, int64_t kv_off,
+                  int causal, float scale, const lsx_tensor& o,
+                  const lsx_tensor& lse, int accumulate, const DeviceCtx& ctx,
+                  cudaStream_t s) {
+  if (q.D == 128)
+    return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse,
+                                accumulate, ctx, s);
+  if (q.D == 64)
+    return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse,
+                               accumulate, ctx, s);
+  return LSX_ERR_UNSUPPORTED;
+}
+
+}  // namespace lsx

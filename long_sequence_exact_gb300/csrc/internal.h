@@ -1,0 +1,126 @@
+// internal.h -- declarations shared by the translation units of liblsx.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lsx.h"
+
+namespace lsx {
+
+// Per-device facts the launchers need.
+struct DeviceCtx {
+  int device;
+  int sm_count;
+  int* status;        // device address of this device's status word
+  uint64_t wait_ns;   // bound of every device-side wait
+};
+
+// Fills ctx for the current device; returns LSX_OK or LSX_ERR_DEVICE.
+int device_ctx(DeviceCtx* ctx);
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Element offset of (b, h, n, 0) in a view.
+__host__ __device__ inline int64_t view_off(const lsx_tensor& t, int64_t b,
+                                            int64_t h, int64_t n) {
+  return b * t.stride_b + h * t.stride_h + n * t.stride_n;
+}
+
+// ----------------------------------------------------------- launchers
+// All launchers assume validated arguments and return LSX_OK or
+// LSX_ERR_LAUNCH.
+
+// O/LSE merge of two partials (attn_merge).
+int launch_merge(const lsx_tensor& oa, const lsx_tensor& la,
+                 const lsx_tensor& ob, const lsx_tensor& lb,
+                 const lsx_tensor& oo, const lsx_tensor& lo,
+                 const DeviceCtx& ctx, cudaStream_t s);
+
+// One-pass merge of n_parts partials (attn_tree_merge).
+int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
+                      int64_t psl, int n_parts, const lsx_tensor& oo,
+                      const lsx_tensor& lo, const DeviceCtx& ctx,
+                      cudaStream_t s);
+
+// delta[b,h,n] = <dO[b,h,n,:], O[b,h,n,:]> into a dense f32 [B*H*N] buffer.
+int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
+                   const DeviceCtx& ctx, cudaStream_t s);
+
+// Writes O = 0 and LSE = -inf for every row (a pair with no visible key);
+// with accumulate the outputs are left as they are (the merge identity).
+int launch_fill_empty(const lsx_tensor& o, const lsx_tensor& lse,
+                      const DeviceCtx& ctx, cudaStream_t s);
+
+// Zero a [B,H,N,D] view (used for gradients of keys nobody sees).
+int launch_zero(const lsx_tensor& t, const DeviceCtx& ctx, cudaStream_t s);
+
+// fp32 CUDA-core path (f32 inputs).
+int launch_simt_fwd(const lsx_tensor& q, const lsx_tensor& k,
+                    const lsx_tensor& v, int64_t q_off, int64_t kv_off,
+                    int causal, float scale, const lsx_tensor& o,
+                    const lsx_tensor& lse, int accumulate, const DeviceCtx& ctx,
+                    cudaStream_t s);
+int launch_simt_bwd(const lsx_tensor& q, const lsx_tensor& k,
+                    const lsx_tensor& v, const lsx_tensor& lse,
+                    const lsx_tensor& d_o, const float* delta, int64_t q_off,
+                    int64_t kv_off, int causal, float scale,
+                    const lsx_tensor& dq, const lsx_tensor& dk,
+                    const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
+                    cudaStream_t s);
+
+// tcgen05 tensor-core forward (bf16 inputs).
+int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
+                  const lsx_tensor& v, int64_t q_off, int64_t kv_off,
+                  int causal, float scale, const lsx_tensor& o,
+                  const lsx_tensor& lse, int accumulate, const DeviceCtx& ctx,
+                  cudaStream_t s);
+
+// tcgen05 tensor-core backward (bf16 inputs).
+int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k,
+                  const lsx_tensor& v, const lsx_tensor& lse,
+                  const lsx_tensor& d_o, const float* delta, int64_t q_off,
+                  int64_t kv_off, int causal, float scale,
+                  const lsx_tensor& dq, const lsx_tensor& dk,
+                  const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
+                  cudaStream_t s);
+
+// Split-KV decode partials (bf16 inputs, D = 128).
+int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
+                           const lsx_tensor& vc, int64_t chunk_len,
+                           float scale, float* part_o, float* part_lse,
+                           const DeviceCtx& ctx, cudaStream_t s);
+
+// Host-side forward work schedule shared with the forward kernel: the
+// order in which work items are handed to persistent CTAs.
+struct FwdSchedule {
+  int64_t n_items;   // (B * H) * n_qpairs
+  int64_t n_qpairs;  // ceil(Lq / 256)
+  int64_t bh;        // B * H
+};
+
+// KV tiles of 128 keys that query tile t (rows [128 t, 128 t + 128)) must
+// visit.  Shared by host (schedule statistics) and device.
+__host__ __device__ inline int64_t fwd_kv_tiles(int64_t t, int64_t Lq,
+                                                int64_t Lk, int64_t q_off,
+                                                int64_t kv_off, int causal) {
+  const int64_t r0 = t * 128;
+  if (r0 >= Lq) return 0;
+  int64_t kmax = Lk;
+  if (causal) {
+    const int64_t last = (r0 + 127 < Lq - 1 ? r0 + 127 : Lq - 1);
+    const int64_t vis = q_off + last - kv_off + 1;  // keys visible to last row
+    kmax = vis < Lk ? vis : Lk;
+  }
+  return kmax > 0 ? (kmax + 127) / 128 : 0;
+}
+
+// Work item -> (bh, pair) for the persistent forward grid.  Items are in
+// decreasing-cost order (the pair with the most key tiles first); CTA c of G
+// takes, in round r, item r*G + c on even rounds and r*G + (G-1-c) on odd
+// rounds (a "snake" deal that evens out the longest-first order).
+__host__ __device__ inline int64_t snake_item(int64_t c, int64_t r, int64_t G) {
+  return r * G + ((r & 1) ? (G - 1 - c) : c);
+}
+
+}  // namespace lsx

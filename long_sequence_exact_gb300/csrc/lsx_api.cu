@@ -1,0 +1,459 @@
+// lsx_api.cu -- the C ABI declared in include/lsx.h: argument validation,
+// workspace sizing, dispatch to the kernels, the device status word and the
+// host-side diagnostics.  Every check runs before any launch, so a call that
+// returns an error has touched nothing.
+#include <math.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <vector>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace lsx {
+
+// One status word per device that loads the library.
+__device__ int g_status_word;
+
+namespace {
+
+constexpr uint64_t kDefaultWaitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+
+struct DevCache {
+  bool ready = false;
+  int sm_count = 0;
+  int* status = nullptr;
+};
+std::mutex g_mu;
+std::vector<DevCache> g_devs;
+
+}  // namespace
+
+int device_ctx(DeviceCtx* ctx) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return LSX_ERR_DEVICE;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (static_cast<int>(g_devs.size()) <= dev) g_devs.resize(dev + 1);
+  DevCache& dc = g_devs[dev];
+  if (!dc.ready) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return LSX_ERR_DEVICE;
+    if (prop.major != 10 || prop.minor != 3) return LSX_ERR_DEVICE;  // sm_103 only
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return LSX_ERR_DEVICE;
+    dc.sm_count = prop.multiProcessorCount;
+    dc.status = static_cast<int*>(addr);
+    dc.ready = true;
+  }
+  ctx->device = dev;
+  ctx->sm_count = dc.sm_count;
+  ctx->status = dc.status;
+  ctx->wait_ns = g_wait_ns.load();
+  return LSX_OK;
+}
+
+namespace {
+
+// ---------------------------------------------------------- validation
+int check_view(const lsx_tensor* t) {
+  if (t == nullptr) return LSX_ERR_NULL;
+  if (t->data == nullptr && t->N != 0) return LSX_ERR_NULL;  // empty views may be NULL
+  if (t->dtype != LSX_BF16 && t->dtype != LSX_F32) return LSX_ERR_DTYPE;
+  if (t->B <= 0 || t->H <= 0 || t->N < 0 || t->D <= 0) return LSX_ERR_SHAPE;
+  if (t->stride_b < 0 || t->stride_h < 0 || t->stride_n < 0) return LSX_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(t->data) % 16 != 0) return LSX_ERR_ALIGN;
+  return LSX_OK;
+}
+
+int elem_size(int dtype) { return dtype == LSX_F32 ? 4 : 2; }
+
+// A row of D elements is read/written with 16-byte vectors (or 8-byte for
+// bf16 rows of 64/128 in the merge kernels): rows must start 16-B aligned.
+int check_row_aligned(const lsx_tensor* t) {
+  const int64_t vec = 16 / elem_size(t->dtype);
+  if (t->stride_n % vec || t->stride_h % vec || t->stride_b % vec) return LSX_ERR_ALIGN;
+  return LSX_OK;
+}
+
+int check_lse(const lsx_tensor* l, const lsx_tensor* like) {
+  if (l == nullptr || l->data == nullptr) return LSX_ERR_NULL;
+  if (l->dtype != LSX_F32) return LSX_ERR_DTYPE;
+  if (l->D != 1 || l->B != like->B || l->H != like->H || l->N != like->N) return LSX_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(l->data) % 4 != 0) return LSX_ERR_ALIGN;
+  if (l->stride_b < 0 || l->stride_h < 0 || l->stride_n < 0) return LSX_ERR_SHAPE;
+  return LSX_OK;
+}
+
+bool same_bhn_d(const lsx_tensor* a, const lsx_tensor* b) {
+  return a->B == b->B && a->H == b->H && a->N == b->N && a->D == b->D;
+}
+
+#define LSX_TRY(expr)          \
+  do {                         \
+    const int _rc = (expr);    \
+    if (_rc != LSX_OK) return _rc; \
+  } while (0)
+
+// q [B,Hq,Lq,D], k/v [B,Hkv,Lk,D], same dtype, D in {64,128}, Hq % Hkv == 0.
+int check_qkv(const lsx_tensor* q, const lsx_tensor* k, const lsx_tensor* v) {
+  LSX_TRY(check_view(q));
+  LSX_TRY(check_view(k));
+  LSX_TRY(check_view(v));
+  if (k->dtype != q->dtype || v->dtype != q->dtype) return LSX_ERR_DTYPE;
+  if (k->B != q->B || v->B != q->B || k->D != q->D || v->D != q->D ||
+      v->H != k->H || v->N != k->N)
+    return LSX_ERR_SHAPE;
+  if (q->H % k->H != 0) return LSX_ERR_SHAPE;
+  if (q->D != 64 && q->D != 128) return LSX_ERR_UNSUPPORTED;
+  LSX_TRY(check_row_aligned(q));
+  LSX_TRY(check_row_aligned(k));
+  LSX_TRY(check_row_aligned(v));
+  // TMA: every coordinate must fit a 32-bit signed integer
+  const int64_t lim = int64_t(1) << 31;
+  if (q->N >= lim || k->N >= lim || q->H >= lim || q->B >= lim) return LSX_ERR_UNSUPPORTED;
+  return LSX_OK;
+}
+
+float resolve_scale(float scale, int64_t d) {
+  return scale > 0.f ? scale : 1.f / sqrtf(static_cast<float>(d));
+}
+
+cudaStream_t as_stream(lsx_stream_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+}  // namespace
+}  // namespace lsx
+
+using namespace lsx;
+
+extern "C" {
+
+const char* lsx_version(void) { return "lsx 0.1 sm_103a"; }
+
+const char* lsx_status_string(int code) {
+  switch (code) {
+    case LSX_OK: return "ok";
+    case LSX_ERR_NULL: return "null pointer";
+    case LSX_ERR_SHAPE: return "shape mismatch";
+    case LSX_ERR_DTYPE: return "unsupported dtype combination";
+    case LSX_ERR_ALIGN: return "misaligned base or stride";
+    case LSX_ERR_UNSUPPORTED: return "unsupported size or option";
+    case LSX_ERR_WORKSPACE: return "workspace missing or too small";
+    case LSX_ERR_LAUNCH: return "CUDA launch or API failure";
+    case LSX_ERR_TIMEOUT: return "device-side bounded wait ran out";
+    case LSX_ERR_DEVICE: return "no usable sm_103 device";
+    default: return "unknown status";
+  }
+}
+
+void lsx_set_wait_limit_ns(uint64_t ns) {
+  g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
+}
+
+int lsx_sync_status(lsx_stream_t stream) {
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return LSX_ERR_LAUNCH;
+  int word = 0;
+  if (cudaMemcpy(&word, ctx.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LSX_ERR_LAUNCH;
+  const int zero = 0;
+  if (cudaMemcpy(ctx.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return LSX_ERR_LAUNCH;
+  return word;
+}
+
+// ------------------------------------------------------------ attn_merge
+int attn_merge(const lsx_tensor* o_a, const lsx_tensor* lse_a,
+               const lsx_tensor* o_b, const lsx_tensor* lse_b,
+               const lsx_tensor* o_out, const lsx_tensor* lse_out,
+               lsx_stream_t stream) {
+  LSX_TRY(check_view(o_a));
+  LSX_TRY(check_view(o_b));
+  LSX_TRY(check_view(o_out));
+  if (!same_bhn_d(o_a, o_b) || !same_bhn_d(o_a, o_out)) return LSX_ERR_SHAPE;
+  if (o_a->D != 64 && o_a->D != 128) return LSX_ERR_UNSUPPORTED;
+  LSX_TRY(check_row_aligned(o_a));
+  LSX_TRY(check_row_aligned(o_b));
+  LSX_TRY(check_row_aligned(o_out));
+  LSX_TRY(check_lse(lse_a, o_a));
+  LSX_TRY(check_lse(lse_b, o_a));
+  LSX_TRY(check_lse(lse_out, o_a));
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  return launch_merge(*o_a, *lse_a, *o_b, *lse_b, *o_out, *lse_out, ctx,
+                      as_stream(stream));
+}
+
+// ------------------------------------------------------- attn_tree_merge
+int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
+                    const lsx_tensor* lse_parts, int64_t part_stride_lse,
+                    int n_parts, const lsx_tensor* o_out,
+                    const lsx_tensor* lse_out, lsx_stream_t stream) {
+  LSX_TRY(check_view(o_parts));
+  LSX_TRY(check_view(o_out));
+  if (!same_bhn_d(o_parts, o_out)) return LSX_ERR_SHAPE;
+  if (o_parts->D != 64 && o_parts->D != 128) return LSX_ERR_UNSUPPORTED;
+  if (n_parts < 1 || n_parts > 4096) return LSX_ERR_UNSUPPORTED;
+  if (part_stride_o < 0 || part_stride_lse < 0) return LSX_ERR_SHAPE;
+  LSX_TRY(check_row_aligned(o_parts));
+  LSX_TRY(check_row_aligned(o_out));
+  if (part_stride_o % (16 / elem_size(o_parts->dtype)) != 0) return LSX_ERR_ALIGN;
+  LSX_TRY(check_lse(lse_parts, o_parts));
+  lsx_tensor lo_none{};
+  const lsx_tensor* lo = lse_out;
+  if (lse_out == nullptr || lse_out->data == nullptr) {
+    lo_none = *o_out;
+    lo_none.data = nullptr;
+    lo_none.D = 1;
+    lo = &lo_none;
+  } else {
+    LSX_TRY(check_lse(lse_out, o_parts));
+  }
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  return launch_tree_merge(*o_parts, part_stride_o, *lse_parts, part_stride_lse,
+                           n_parts, *o_out, *lo, ctx, as_stream(stream));
+}
+
+// -------------------------------------------------------- attn_chunk_fwd
+int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
+                   const lsx_tensor* v, int64_t q_off, int64_t kv_off,
+                   int causal, float scale, const lsx_tensor* o,
+                   const lsx_tensor* lse, int accumulate, void* workspace,
+                   size_t workspace_bytes, lsx_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  LSX_TRY(check_qkv(q, k, v));
+  LSX_TRY(check_view(o));
+  if (o->B != q->B || o->H != q->H || o->N != q->N || o->D != q->D) return LSX_ERR_SHAPE;
+  if (q->dtype == LSX_F32 && o->dtype != LSX_F32) return LSX_ERR_DTYPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_lse(lse, q));
+  if (q_off < 0 || kv_off < 0) return LSX_ERR_SHAPE;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const float sc = resolve_scale(scale, q->D);
+  cudaStream_t s = as_stream(stream);
+  if (q->N == 0) return LSX_OK;
+  if (k->N == 0) return accumulate ? LSX_OK : launch_fill_empty(*o, *lse, ctx, s);
+  if (q->dtype == LSX_F32)
+    return launch_simt_fwd(*q, *k, *v, q_off, kv_off, causal != 0, sc, *o, *lse,
+                           accumulate != 0, ctx, s);
+  return launch_fwd_tc(*q, *k, *v, q_off, kv_off, causal != 0, sc, *o, *lse,
+                       accumulate != 0, ctx, s);
+}
+
+// -------------------------------------------------------- attn_chunk_bwd
+size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+  (void)k;
+  if (q == nullptr) return 0;
+  const int64_t rows = q->B * q->H * q->N;
+  return static_cast<size_t>(rows > 0 ? rows : 0) * sizeof(float) + 256;
+}
+
+int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
+                   const lsx_tensor* v, const lsx_tensor* o,
+                   const lsx_tensor* lse, const lsx_tensor* d_o,
+                   int64_t q_off, int64_t kv_off, int causal, float scale,
+                   const lsx_tensor* dq, const lsx_tensor* dk,
+                   const lsx_tensor* dv, int accumulate, void* workspace,
+                   size_t workspace_bytes, lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, k, v));
+  LSX_TRY(check_view(o));
+  LSX_TRY(check_view(d_o));
+  LSX_TRY(check_view(dq));
+  LSX_TRY(check_view(dk));
+  LSX_TRY(check_view(dv));
+  if (!same_bhn_d(o, q) || !same_bhn_d(d_o, q) || !same_bhn_d(dq, q) ||
+      !same_bhn_d(dk, k) || !same_bhn_d(dv, k))
+    return LSX_ERR_SHAPE;
+  if (d_o->dtype != q->dtype) return LSX_ERR_DTYPE;
+  if (q->dtype == LSX_F32 &&
+      (dq->dtype != LSX_F32 || dk->dtype != LSX_F32 || dv->dtype != LSX_F32 ||
+       o->dtype != LSX_F32))
+    return LSX_ERR_DTYPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_row_aligned(d_o));
+  LSX_TRY(check_row_aligned(dq));
+  LSX_TRY(check_row_aligned(dk));
+  LSX_TRY(check_row_aligned(dv));
+  LSX_TRY(check_lse(lse, q));
+  if (q_off < 0 || kv_off < 0) return LSX_ERR_SHAPE;
+  const size_t need = attn_chunk_bwd_workspace_size(q, k);
+  if (workspace == nullptr || workspace_bytes < need) return LSX_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const float sc = resolve_scale(scale, q->D);
+  cudaStream_t s = as_stream(stream);
+  if (q->N == 0 || k->N == 0) {
+    if (accumulate) return LSX_OK;
+    if (q->N > 0) LSX_TRY(launch_zero(*dq, ctx, s));
+    if (k->N > 0) {
+      LSX_TRY(launch_zero(*dk, ctx, s));
+      LSX_TRY(launch_zero(*dv, ctx, s));
+    }
+    return LSX_OK;
+  }
+  float* delta = static_cast<float*>(workspace);
+  LSX_TRY(launch_row_dot(*o, *d_o, delta, ctx, s));
+  if (q->dtype == LSX_F32)
+    return launch_simt_bwd(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off,
+                           causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
+  return launch_bwd_tc(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off, causal != 0,
+                       sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
+}
+
+// ------------------------------------------- whole-sequence chunked calls
+size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
+                                       int64_t chunk_len, int causal) {
+  (void)q; (void)k; (void)chunk_len; (void)causal;
+  return 0;
+}
+
+int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
+                     const lsx_tensor* v, int64_t chunk_len, int causal,
+                     float scale, const lsx_tensor* o, const lsx_tensor* lse,
+                     void* workspace, size_t workspace_bytes,
+                     lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, k, v));
+  if (q->N != k->N) return LSX_ERR_SHAPE;
+  if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  // One persistent launch covers every visible chunk pair (see fwd_tc.cu);
+  // the chunk length sets no boundary the online softmax could not cross.
+  return attn_chunk_fwd(q, k, v, 0, 0, causal, scale, o, lse, 0, workspace,
+                        workspace_bytes, stream);
+}
+
+size_t attn_chunked_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
+                                       int64_t chunk_len, int causal) {
+  (void)chunk_len; (void)causal;
+  return attn_chunk_bwd_workspace_size(q, k);
+}
+
+int attn_chunked_bwd(const lsx_tensor* q, const lsx_tensor* k,
+                     const lsx_tensor* v, const lsx_tensor* o,
+                     const lsx_tensor* lse, const lsx_tensor* d_o,
+                     int64_t chunk_len, int causal, float scale,
+                     const lsx_tensor* dq, const lsx_tensor* dk,
+                     const lsx_tensor* dv, void* workspace,
+                     size_t workspace_bytes, lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, k, v));
+  if (q->N != k->N) return LSX_ERR_SHAPE;
+  if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  return attn_chunk_bwd(q, k, v, o, lse, d_o, 0, 0, causal, scale, dq, dk, dv, 0,
+                        workspace, workspace_bytes, stream);
+}
+
+// ----------------------------------------------------------- attn_decode
+size_t attn_decode_workspace_size(const lsx_tensor* q, const lsx_tensor* kc,
+                                  int64_t chunk_len) {
+  if (q == nullptr || kc == nullptr || chunk_len <= 0) return 0;
+  const int64_t parts = ceil_div(kc->N, chunk_len);
+  const int64_t rows = q->B * q->H;
+  // partial O [parts][rows][D] f32, then partial LSE [parts][rows] f32
+  const size_t o_bytes = static_cast<size_t>(parts * rows * q->D) * sizeof(float);
+  const size_t l_bytes = static_cast<size_t>(parts * rows) * sizeof(float);
+  return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+}
+
+int attn_decode(const lsx_tensor* q, const lsx_tensor* kc,
+                const lsx_tensor* vc, int64_t chunk_len, float scale,
+                const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                size_t workspace_bytes, lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, kc, vc));
+  if (q->dtype != LSX_BF16) return LSX_ERR_DTYPE;
+  if (q->N != 1 || q->D != 128) return LSX_ERR_UNSUPPORTED;
+  {
+    const int64_t g = q->H / kc->H;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return LSX_ERR_UNSUPPORTED;
+  }
+  LSX_TRY(check_view(o));
+  if (!same_bhn_d(o, q)) return LSX_ERR_SHAPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_lse(lse, q));
+  if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  const int64_t parts = ceil_div(kc->N, chunk_len);
+  if (parts > 4096) return LSX_ERR_UNSUPPORTED;
+  const size_t need = attn_decode_workspace_size(q, kc, chunk_len);
+  if (workspace == nullptr || workspace_bytes < need) return LSX_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  cudaStream_t s = as_stream(stream);
+  if (kc->N == 0) return launch_fill_empty(*o, *lse, ctx, s);
+  const float sc = resolve_scale(scale, q->D);
+  const int64_t rows = q->B * q->H;
+  float* part_o = static_cast<float*>(workspace);
+  const size_t o_bytes = static_cast<size_t>(parts * rows * q->D) * sizeof(float);
+  float* part_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           ((o_bytes + 255) / 256) * 256);
+  LSX_TRY(launch_decode_partials(*q, *kc, *vc, chunk_len, sc, part_o, part_l, ctx, s));
+  // partial p of query row (b, h) sits at part_o[(p * rows + b*H + h) * D]
+  lsx_tensor po{part_o, LSX_F32, 0, q->B, q->H, 1, q->D, q->H * q->D, q->D, q->D};
+  lsx_tensor pl{part_l, LSX_F32, 0, q->B, q->H, 1, 1, q->H, 1, 1};
+  return launch_tree_merge(po, rows * q->D, pl, rows, static_cast<int>(parts), *o,
+                           *lse, ctx, s);
+}
+
+// ------------------------------------------------------------ diagnostics
+int lsx_schedule_stats(int64_t B, int64_t H, int64_t N, int64_t chunk_len,
+                       int causal, int n_workers, int64_t* out) {
+  if (out == nullptr) return LSX_ERR_NULL;
+  if (B <= 0 || H <= 0 || N <= 0 || n_workers <= 0) return LSX_ERR_SHAPE;
+  if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  const int64_t n_qpairs = ceil_div(N, 256);
+  const int64_t n_items = n_qpairs * B * H;
+  const int64_t G = n_items < n_workers ? n_items : n_workers;
+  std::vector<int64_t> load(static_cast<size_t>(G), 0);
+  int64_t total = 0;
+  for (int64_t c = 0; c < G; ++c) {
+    for (int64_t r = 0;; ++r) {
+      const int64_t it = snake_item(c, r, G);
+      if (it >= n_items) break;
+      const int64_t pair = n_qpairs - 1 - it / (B * H);
+      const int64_t a = fwd_kv_tiles(2 * pair, N, N, 0, 0, causal);
+      const int64_t b = fwd_kv_tiles(2 * pair + 1, N, N, 0, 0, causal);
+      const int64_t cost = a + b;  // one S and one P.V product per tile row
+      load[static_cast<size_t>(c)] += cost;
+      total += cost;
+    }
+  }
+  out[0] = *std::max_element(load.begin(), load.end());
+  out[1] = ceil_div(total, n_workers);
+  out[2] = total;
+  return LSX_OK;
+}
+
+}  // extern "C"
+
+// ------------------------------------------------ bounded-wait self-test
+namespace lsx {
+namespace {
+__global__ void bounded_wait_kernel(int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);  // nobody ever arrives
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const WaitGuard g{status, limit_ns, &abort_flag};
+  (void)mbar_wait(&bar, 0, g);
+  __syncthreads();
+}
+}  // namespace
+}  // namespace lsx
+
+extern "C" int lsx_selftest_bounded_wait(lsx_stream_t stream) {
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  bounded_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(ctx.status, ctx.wait_ns);
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}

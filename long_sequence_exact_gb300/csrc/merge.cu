@@ -1,0 +1,357 @@
+// merge.cu -- bandwidth-bound kernels: the pairwise LSE merge, the one-pass
+// k-way merge, the backward row dot product and small fills.
+//
+// Merge rule (BurstAttention abstract: local results aggregated into global
+// ones; Lean Attention abstract: online softmax is associative, so the
+// combination is a reduction; Tree Attention abstract: the reduction across
+// the sequence axis is a tree reduction):
+//   m = max_p LSE_p,  w_p = exp(LSE_p - m),  LSE = m + log sum_p w_p,
+//   O = sum_p (w_p / sum w) O_p;   all LSE_p = -inf  ->  O = 0, LSE = -inf.
+//
+// Layout: one warp per row of D elements; lane l owns elements
+// [l*E, l*E + E) with E = D / 32, so each row is one fully coalesced access
+// per tensor.  Grids are sized in multiples of the SM count.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "internal.h"
+
+namespace lsx {
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+template <int E>
+struct Vec {
+  float v[E];
+};
+
+template <int E>
+__device__ __forceinline__ Vec<E> load_row(const void* base, int dtype,
+                                           int64_t off, int lane) {
+  Vec<E> r;
+  if (dtype == LSX_F32) {
+    const float* p = static_cast<const float*>(base) + off + lane * E;
+    if constexpr (E == 4) {
+      float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+      r.v[0] = x.x; r.v[1] = x.y; r.v[2] = x.z; r.v[3] = x.w;
+    } else if constexpr (E == 2) {
+      float2 x = __ldcs(reinterpret_cast<const float2*>(p));
+      r.v[0] = x.x; r.v[1] = x.y;
+    } else {
+      for (int e = 0; e < E; ++e) r.v[e] = p[e];
+    }
+  } else {
+    const __nv_bfloat16* p =
+        static_cast<const __nv_bfloat16*>(base) + off + lane * E;
+    if constexpr (E == 4) {
+      uint2 x = __ldcs(reinterpret_cast<const uint2*>(p));
+      __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x.x);
+      __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&x.y);
+      r.v[0] = __low2float(a); r.v[1] = __high2float(a);
+      r.v[2] = __low2float(b); r.v[3] = __high2float(b);
+    } else if constexpr (E == 2) {
+      uint32_t x = __ldcs(reinterpret_cast<const unsigned int*>(p));
+      __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&x);
+      r.v[0] = __low2float(a); r.v[1] = __high2float(a);
+    } else {
+      for (int e = 0; e < E; ++e) r.v[e] = __bfloat162float(p[e]);
+    }
+  }
+  return r;
+}
+
+template <int E>
+__device__ __forceinline__ void store_row(void* base, int dtype, int64_t off,
+                                          int lane, const Vec<E>& r) {
+  if (dtype == LSX_F32) {
+    float* p = static_cast<float*>(base) + off + lane * E;
+    if constexpr (E == 4) {
+      __stcs(reinterpret_cast<float4*>(p),
+             make_float4(r.v[0], r.v[1], r.v[2], r.v[3]));
+    } else if constexpr (E == 2) {
+      __stcs(reinterpret_cast<float2*>(p), make_float2(r.v[0], r.v[1]));
+    } else {
+      for (int e = 0; e < E; ++e) p[e] = r.v[e];
+    }
+  } else {
+    __nv_bfloat16* p = static_cast<__nv_bfloat16*>(base) + off + lane * E;
+    if constexpr (E == 4) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(r.v[0], r.v[1]);
+      __nv_bfloat162 b = __floats2bfloat162_rn(r.v[2], r.v[3]);
+      uint2 x;
+      x.x = *reinterpret_cast<uint32_t*>(&a);
+      x.y = *reinterpret_cast<uint32_t*>(&b);
+      __stcs(reinterpret_cast<uint2*>(p), x);
+    } else if constexpr (E == 2) {
+      __nv_bfloat162 a = __floats2bfloat162_rn(r.v[0], r.v[1]);
+      __stcs(reinterpret_cast<unsigned int*>(p),
+             *reinterpret_cast<unsigned int*>(&a));
+    } else {
+      for (int e = 0; e < E; ++e) p[e] = __float2bfloat16_rn(r.v[e]);
+    }
+  }
+}
+
+struct RowIdx {
+  int64_t H, N;
+  __device__ __forceinline__ void split(int64_t row, int64_t& b, int64_t& h,
+                                        int64_t& n) const {
+    n = row % N;
+    const int64_t bh = row / N;
+    h = bh % H;
+    b = bh / H;
+  }
+};
+
+// ------------------------------------------------------------ pairwise
+template <int E>
+__global__ void __launch_bounds__(256) merge_kernel(
+    lsx_tensor oa, lsx_tensor la, lsx_tensor ob, lsx_tensor lb, lsx_tensor oo,
+    lsx_tensor lo, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const RowIdx ri{oa.H, oa.N};
+  const float* pla = static_cast<const float*>(la.data);
+  const float* plb = static_cast<const float*>(lb.data);
+  float* plo = static_cast<float*>(lo.data);
+  for (int64_t row = w0; row < rows; row += nw) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    const float xa = pla[view_off(la, b, h, n)];
+    const float xb = plb[view_off(lb, b, h, n)];
+    const Vec<E> va = load_row<E>(oa.data, oa.dtype, view_off(oa, b, h, n), lane);
+    const Vec<E> vb = load_row<E>(ob.data, ob.dtype, view_off(ob, b, h, n), lane);
+    const float m = fmaxf(xa, xb);
+    Vec<E> out;
+    float l;
+    if (m == kNegInf) {
+      for (int e = 0; e < E; ++e) out.v[e] = 0.f;
+      l = kNegInf;
+    } else {
+      const float wa = expf(xa - m), wb = expf(xb - m);
+      const float tot = wa + wb;
+      const float ra = wa / tot, rb = wb / tot;
+      for (int e = 0; e < E; ++e) out.v[e] = ra * va.v[e] + rb * vb.v[e];
+      l = m + logf(tot);
+    }
+    // all lanes have read their inputs before any store (outputs may alias)
+    __syncwarp();
+    store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, out);
+    if (lane == 0) plo[view_off(lo, b, h, n)] = l;
+  }
+}
+
+// ------------------------------------------------------------- k-way
+// One warp per row; partials are taken in order p = 0, 1, ..., n-1 so the
+// result does not depend on the launch shape.
+template <int E>
+__global__ void __launch_bounds__(256) tree_merge_warp_kernel(
+    lsx_tensor op, int64_t pso, lsx_tensor lp, int64_t psl, int n_parts,
+    lsx_tensor oo, lsx_tensor lo, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const RowIdx ri{op.H, op.N};
+  const float* plp = static_cast<const float*>(lp.data);
+  for (int64_t row = w0; row < rows; row += nw) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    const int64_t lbase = view_off(lp, b, h, n);
+    const int64_t obase = view_off(op, b, h, n);
+    float m = kNegInf;
+    for (int p = lane; p < n_parts; p += 32) m = fmaxf(m, plp[lbase + p * psl]);
+    for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    Vec<E> acc;
+    for (int e = 0; e < E; ++e) acc.v[e] = 0.f;
+    float tot = 0.f;
+    if (m != kNegInf) {
+      for (int p = 0; p < n_parts; ++p) {
+        const float w = expf(plp[lbase + p * psl] - m);
+        const Vec<E> x = load_row<E>(op.data, op.dtype, obase + p * pso, lane);
+        tot += w;
+        for (int e = 0; e < E; ++e) acc.v[e] = fmaf(w, x.v[e], acc.v[e]);
+      }
+      const float inv = 1.f / tot;
+      for (int e = 0; e < E; ++e) acc.v[e] *= inv;
+    }
+    store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, acc);
+    if (lane == 0 && lo.data != nullptr)
+      static_cast<float*>(lo.data)[view_off(lo, b, h, n)] =
+          (m == kNegInf) ? kNegInf : m + logf(tot);
+  }
+}
+
+// One block of 8 warps per row for many partials: warp w takes partials
+// p = w, w + 8, ...; the 8 warp sums are combined in warp order.
+template <int E>
+__global__ void __launch_bounds__(256) tree_merge_block_kernel(
+    lsx_tensor op, int64_t pso, lsx_tensor lp, int64_t psl, int n_parts,
+    lsx_tensor oo, lsx_tensor lo, int64_t rows) {
+  __shared__ float s_max[8];
+  __shared__ float s_tot[8];
+  __shared__ float s_acc[8][32 * E];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const RowIdx ri{op.H, op.N};
+  const float* plp = static_cast<const float*>(lp.data);
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    const int64_t lbase = view_off(lp, b, h, n);
+    const int64_t obase = view_off(op, b, h, n);
+    float m = kNegInf;
+    for (int p = threadIdx.x; p < n_parts; p += blockDim.x)
+      m = fmaxf(m, plp[lbase + p * psl]);
+    for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    if (lane == 0) s_max[warp] = m;
+    __syncthreads();
+    m = s_max[0];
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, s_max[w]);
+    Vec<E> acc;
+    for (int e = 0; e < E; ++e) acc.v[e] = 0.f;
+    float tot = 0.f;
+    if (m != kNegInf) {
+      for (int p = warp; p < n_parts; p += 8) {
+        const float w = expf(plp[lbase + p * psl] - m);
+        const Vec<E> x = load_row<E>(op.data, op.dtype, obase + p * pso, lane);
+        tot += w;
+        for (int e = 0; e < E; ++e) acc.v[e] = fmaf(w, x.v[e], acc.v[e]);
+      }
+    }
+    for (int e = 0; e < E; ++e) s_acc[warp][lane * E + e] = acc.v[e];
+    if (lane == 0) s_tot[warp] = tot;
+    __syncthreads();
+    if (warp == 0) {
+      Vec<E> out;
+      float t = 0.f;
+      for (int e = 0; e < E; ++e) out.v[e] = 0.f;
+      for (int w = 0; w < 8; ++w) {
+        t += s_tot[w];
+        for (int e = 0; e < E; ++e) out.v[e] += s_acc[w][lane * E + e];
+      }
+      if (m != kNegInf) {
+        const float inv = 1.f / t;
+        for (int e = 0; e < E; ++e) out.v[e] *= inv;
+      }
+      store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, out);
+      if (lane == 0 && lo.data != nullptr)
+        static_cast<float*>(lo.data)[view_off(lo, b, h, n)] =
+            (m == kNegInf) ? kNegInf : m + logf(t);
+    }
+    __syncthreads();
+  }
+}
+
+// ----------------------------------------------------------- row dot
+template <int E>
+__global__ void __launch_bounds__(256) row_dot_kernel(lsx_tensor o,
+                                                      lsx_tensor d_o,
+                                                      float* delta,
+                                                      int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const RowIdx ri{o.H, o.N};
+  for (int64_t row = w0; row < rows; row += nw) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    const Vec<E> x = load_row<E>(o.data, o.dtype, view_off(o, b, h, n), lane);
+    const Vec<E> y = load_row<E>(d_o.data, d_o.dtype, view_off(d_o, b, h, n), lane);
+    float s = 0.f;
+    for (int e = 0; e < E; ++e) s = fmaf(x.v[e], y.v[e], s);
+    for (int k = 16; k > 0; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
+    if (lane == 0) delta[row] = s;
+  }
+}
+
+// -------------------------------------------------------------- fills
+template <int E>
+__global__ void __launch_bounds__(256) fill_kernel(lsx_tensor o,
+                                                   lsx_tensor lse,
+                                                   int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const RowIdx ri{o.H, o.N};
+  Vec<E> z;
+  for (int e = 0; e < E; ++e) z.v[e] = 0.f;
+  for (int64_t row = w0; row < rows; row += nw) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    store_row<E>(o.data, o.dtype, view_off(o, b, h, n), lane, z);
+    if (lane == 0 && lse.data != nullptr)
+      static_cast<float*>(lse.data)[view_off(lse, b, h, n)] = kNegInf;
+  }
+}
+
+int grid_for_rows(int64_t rows, const DeviceCtx& ctx, int warps_per_block) {
+  const int64_t blocks = ceil_div(rows, warps_per_block);
+  const int64_t cap = static_cast<int64_t>(ctx.sm_count) * 8;  // 8 x 256 threads per SM
+  return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+#define LSX_DISPATCH_E(D, ...)                     \
+  switch (D) {                                     \
+    case 128: { constexpr int E = 4; __VA_ARGS__; break; } \
+    case 64: { constexpr int E = 2; __VA_ARGS__; break; }  \
+    default: return LSX_ERR_UNSUPPORTED;           \
+  }
+
+int launch_merge(const lsx_tensor& oa, const lsx_tensor& la,
+                 const lsx_tensor& ob, const lsx_tensor& lb,
+                 const lsx_tensor& oo, const lsx_tensor& lo,
+                 const DeviceCtx& ctx, cudaStream_t s) {
+  const int64_t rows = oa.B * oa.H * oa.N;
+  if (rows == 0) return LSX_OK;
+  const int grid = grid_for_rows(rows, ctx, 8);
+  LSX_DISPATCH_E(oa.D, merge_kernel<E><<<grid, 256, 0, s>>>(oa, la, ob, lb, oo, lo, rows));
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
+                      int64_t psl, int n_parts, const lsx_tensor& oo,
+                      const lsx_tensor& lo, const DeviceCtx& ctx,
+                      cudaStream_t s) {
+  const int64_t rows = op.B * op.H * op.N;
+  if (rows == 0) return LSX_OK;
+  if (n_parts <= 16) {
+    const int grid = grid_for_rows(rows, ctx, 8);
+    LSX_DISPATCH_E(op.D, tree_merge_warp_kernel<E><<<grid, 256, 0, s>>>(
+                             op, pso, lp, psl, n_parts, oo, lo, rows));
+  } else {
+    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * 8;
+    const int grid = static_cast<int>(rows < cap ? rows : cap);
+    LSX_DISPATCH_E(op.D, tree_merge_block_kernel<E><<<grid, 256, 0, s>>>(
+                             op, pso, lp, psl, n_parts, oo, lo, rows));
+  }
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
+                   const DeviceCtx& ctx, cudaStream_t s) {
+  const int64_t rows = o.B * o.H * o.N;
+  if (rows == 0) return LSX_OK;
+  const int grid = grid_for_rows(rows, ctx, 8);
+  LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid, 256, 0, s>>>(o, d_o, delta, rows));
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+int launch_fill_empty(const lsx_tensor& o, const lsx_tensor& lse,
+                      const DeviceCtx& ctx, cudaStream_t s) {
+  const int64_t rows = o.B * o.H * o.N;
+  if (rows == 0) return LSX_OK;
+  const int grid = grid_for_rows(rows, ctx, 8);
+  LSX_DISPATCH_E(o.D, fill_kernel<E><<<grid, 256, 0, s>>>(o, lse, rows));
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+int launch_zero(const lsx_tensor& t, const DeviceCtx& ctx, cudaStream_t s) {
+  lsx_tensor none = t;
+  none.data = nullptr;
+  return launch_fill_empty(t, none, ctx, s);
+}
+
+}  // namespace lsx

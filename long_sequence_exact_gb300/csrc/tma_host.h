@@ -1,0 +1,55 @@
+// tma_host.h -- host-side construction of TMA tensor maps for [B, H, N, D]
+// bf16 views (D contiguous).  The driver entry point is fetched through the
+// runtime so the library does not link libcuda directly.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace lsx {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  }
+  return fn;
+}
+
+// Tiled map over a bf16 tensor with dims (innermost first) {D, N, H, B} and
+// element strides {1, sn, sh, sb}.  Box = {64, box_rows, 1, 1} with the
+// 128-byte swizzle, so one box is box_rows rows of 128 bytes, matching the
+// K-major / MN-major SW128 shared-memory layouts the MMAs read.  Rows beyond
+// N read as zero.  Returns false when the driver rejects the map.
+inline bool make_map_bf16_4d(CUtensorMap* map, const void* base, int64_t B,
+                             int64_t H, int64_t N, int64_t D, int64_t sb,
+                             int64_t sh, int64_t sn, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  // a stride of an extent-1 dimension is never used; give it a legal value
+  const int64_t esz = 2;
+  if (H == 1) sh = N * sn;
+  if (B == 1) sb = H * sh;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H,
+                        (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(sn * esz), (cuuint64_t)(sh * esz),
+                           (cuuint64_t)(sb * esz)};
+  cuuint32_t box[4] = {64u, box_rows, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace lsx
