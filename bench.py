@@ -1,0 +1,370 @@
+"""Throughput of the hot path: causal bf16 attention forward + backward at 128K
+tokens (B=1, H=32, N=131072, d=128, chunks of 4096), on N GPUs of one node.
+
+One step = attn_chunked_fwd (persistent forward over every visible chunk
+pair) + attn_chunked_bwd (row dot, dK/dV kernel, dQ kernel) on resident,
+seeded synthetic inputs.  Each rank runs its own full problem (the heads and
+sequences of a batch are independent), so N GPUs do N times the work: weak
+scaling, no data-path collective.
+
+FLOP convention: only visible (causal) query-key pairs count; a forward is two
+GEMMs over them (2 * B * H * N^2 * d for the causal square), a backward 2.5x
+that.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  --impl reference times the fp64 oracle on the
+host cores on a bounded sample of the same workload (the reference arm).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal bf16 attn fwd+bwd TFLOP/s at 128K tokens, % of tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "causal_128k_balanced"
+
+
+def flops(b, h, n, d, causal=True):
+    pairs = n * (n + 1) / 2 if causal else n * n
+    fwd = 4.0 * b * h * pairs * d
+    return fwd, 2.5 * fwd
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        return {"hbm_gbs": m["hbm_gbs"], "bf16": m["bf16_tflops"],
+                "bf16_sustained": m["bf16_tflops_sustained"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_times(lib_mod):
+    import ctypes
+    lib = lib_mod.load()
+    buf = ctypes.create_string_buffer(4096)
+    n = lib.lsx_timing_report(buf, 4096)
+    out = {}
+    if n > 0:
+        for line in buf.value.decode().strip().splitlines():
+            name, cnt, tot = line.split()
+            out[name] = (int(cnt), float(tot))
+    return out
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import long_sequence_exact_gb300 as lsx
+    from long_sequence_exact_gb300 import _lib
+    from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = WORKLOADS[WORKLOAD]
+    x = make_inputs(w, device=dev, seed=w.seed + rank)
+    q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    import ctypes
+    vq_, vk_ = _lib.view(q), _lib.view(k)
+    ws_bytes = _lib.load().attn_chunked_bwd_workspace_size(ctypes.byref(vq_), ctypes.byref(vk_),
+                                                           w.chunk, 1)
+    ws = torch.empty(int(ws_bytes), dtype=torch.uint8, device=dev)
+
+    def step():
+        lsx.chunked_fwd(q, k, v, w.chunk, causal=True, out=o, lse=lse)
+        lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=True, dq=dq, dk=dk, dv=dv,
+                        workspace=ws)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if lsx.sync_status() != 0:
+        raise RuntimeError("device status after warm-up")
+
+    lib = _lib.load()
+    lib.lsx_timing_reset()
+    lib.lsx_timing_enable(1)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    lib.lsx_timing_enable(0)
+    ms = e0.elapsed_time(e1)
+    ktimes = kernel_times(_lib)
+    lib.lsx_timing_reset()
+    if lsx.sync_status() != 0:
+        raise RuntimeError("device status after the timed steps")
+
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+
+    f_fwd, f_bwd = flops(w.B, w.Hq, w.N, w.D)
+    step_flops = f_fwd + f_bwd
+    value = world * step_flops * args.steps / (ms_max / 1e3) / 1e12
+
+    # end to end through the same C ABI, inputs copied in from pinned host
+    # memory and every output copied back, each step
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_, hdo = (t_.cpu().pin_memory() for t_ in (q, k, v, d_o))
+        ho, hl = torch.empty_like(o, device="cpu").pin_memory(), torch.empty_like(lse, device="cpu").pin_memory()
+        hdq, hdk, hdv = (torch.empty_like(t_, device="cpu").pin_memory() for t_ in (dq, dk, dv))
+        h2d = sum(t_.numel() * t_.element_size() for t_ in (hq_, hk_, hv_, hdo))
+        d2h = sum(t_.numel() * t_.element_size() for t_ in (ho, hl, hdq, hdk, hdv))
+
+        def e2e_step():
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            d_o.copy_(hdo, non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+            hdq.copy_(dq, non_blocking=True)
+            hdk.copy_(dk, non_blocking=True)
+            hdv.copy_(dv, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        n_e2e = max(1, min(args.steps, 3))
+        for _ in range(n_e2e):
+            e2e_step()
+        b_.record(stream)
+        torch.cuda.synchronize()
+        te = torch.tensor([a.elapsed_time(b_)], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        e2e = {"value": round(world * step_flops * n_e2e / (float(te.item()) / 1e3) / 1e12, 2),
+               "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "steps": n_e2e}
+
+    if rank != 0:
+        return None
+
+    pk = peaks()
+    # dominant kernel by measured time; its algorithmic work per launch:
+    # fwd_tc = the two forward GEMMs; bwd_dkdv_tc = S^T, dP^T, dV, dK (4 of the
+    # 5 backward GEMMs); bwd_dq_tc = dQ (1 of 5; its S and dP are recomputed)
+    unit_gemm = f_fwd / 2.0
+    algo = {"fwd_tc": 2 * unit_gemm, "bwd_dkdv_tc": 4 * unit_gemm, "bwd_dq_tc": 1 * unit_gemm}
+    dom = max(ktimes.items(), key=lambda kv: kv[1][1]) if ktimes else None
+    roofline = None
+    kernels = {}
+    for name, (cnt, tot) in ktimes.items():
+        avg = tot / cnt
+        ent = {"launches": cnt, "avg_ms": round(avg, 4), "share": round(tot / sum(t_[1] for t_ in ktimes.values()), 4)}
+        if name in algo:
+            ach = algo[name] / (avg / 1e3) / 1e12
+            ent["achieved_tflops"] = round(ach, 1)
+            ent["frac_of_peak"] = round(ach / pk["bf16_sustained"], 4)
+        kernels[name] = ent
+    if dom is not None and dom[0] in algo:
+        name, (cnt, tot) = dom
+        ach = algo[name] / (tot / cnt / 1e3) / 1e12
+        roofline = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
+                    "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
+                    "frac": round(ach / pk["bf16_sustained"], 4), "traffic": args.traffic,
+                    "peak_kind": f"{pk['source']} bf16 sustained (kernel timed inside a long step)"}
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        cpu = cpu_baseline(args.cpu_rows)
+
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)*0.5 q/k/v, N(0,1) dO; one problem per rank)",
+        "config": {"workload": WORKLOAD, "B": w.B, "H": w.Hq, "N": w.N, "d": w.D,
+                   "chunk_len": w.chunk, "causal": True,
+                   "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd,
+                   "l2": "inputs larger than L2 (q, k, v, dO 1 GiB each; no flush needed)",
+                   "pct_of_tensor_peak": round(100.0 * value / world / pk["bf16_sustained"], 2)},
+        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": sum(c for c, _ in ktimes.values()),
+        "clocks": clk.summary(),
+    }
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_baseline(rows_per_sample=512, repeats=1):
+    """The fp64 oracle as it stands, on the host cores, on a bounded sample:
+    the last `rows_per_sample` query rows of head 0 of the 128K workload
+    (each sees ~131K keys), forward + backward.  Value in the metric's unit
+    (TFLOP/s by the same visible-pair convention)."""
+    import numpy as np
+    import torch
+
+    from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs
+    from oracle import attention as A
+
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    w = WORKLOADS[WORKLOAD].with_(Hq=1, Hkv=1)
+    x = make_inputs(w, device="cpu")
+    f = lambda t: t.double().numpy()  # noqa: E731
+    q, k, v, d_o = f(x["q"]), f(x["k"]), f(x["v"]), f(x["d_o"])
+    rows = np.arange(w.N - rows_per_sample, w.N)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        A.attn_fwd(q, k, v, 0, 0, True, rows=rows)
+        A.attn_bwd(q, k, v, d_o, 0, 0, True, rows=rows)
+    dt = (time.perf_counter() - t0) / repeats
+    pairs = float(sum(r + 1 for r in rows))
+    fl = 4.0 * pairs * w.D * 3.5  # fwd + 2.5x fwd
+    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 numpy oracle, fwd+bwd of the last {rows_per_sample} query rows of "
+                      f"head 0 (N={w.N}, d={w.D}, causal), {dt:.2f} s",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    cores = len(os.sched_getaffinity(0))
+    for _ in range(args.warmup):
+        cpu_baseline(args.cpu_rows // 4)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(args.cpu_rows))
+    total = time.perf_counter() - t0
+    value = statistics.mean(v["value"] for v in vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "B": 1, "H": 32, "N": 131072,
+                                        "d": 128, "chunk_len": 4096, "causal": True},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores,
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="dram bytes per launch of the dominant kernel from an ncu capture")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        out = run_reference(args, rank)
+    else:
+        if world > 1:
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl")
+        out = run_ours(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

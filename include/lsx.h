@@ -232,6 +232,18 @@ int lsx_schedule_stats(int64_t B, int64_t H, int64_t N, int64_t chunk_len,
 /* Library version string, e.g. "lsx 0.1 sm_103a". */
 const char* lsx_version(void);
 
+/* Per-kernel timing.  While enabled, every kernel launch of the library is
+ * bracketed by a pair of CUDA events recorded on the launching stream (the
+ * events are created by the library on first use; no device memory).
+ * lsx_timing_report synchronises those events and writes, for each kernel
+ * that ran since the last reset, one line "name launches total_ms\n" into
+ * buf (host memory, NUL-terminated, truncated to n bytes); it returns the
+ * number of kernels reported or a negative status.  lsx_timing_reset drops
+ * the recorded events.  Process-wide; not meant for concurrent callers. */
+int lsx_timing_enable(int on);
+int lsx_timing_report(char* buf, size_t n);
+int lsx_timing_reset(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -702,7 +702,9 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    timing_begin(kKidDkdv, s);
     dkdv_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(tq, tk, tv, tdo, p);
+    timing_end(kKidDkdv, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
   // dQ: items (query tile, b, head)
@@ -713,7 +715,9 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    timing_begin(kKidDq, s);
     dq_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(tq, tk, tv, tdo, p);
+    timing_end(kKidDq, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
   return LSX_OK;

@@ -194,6 +194,7 @@ int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
   if (parts > 65535 * 1024LL || kc.H > 65535 || q.B > 65535) return LSX_ERR_UNSUPPORTED;
   dim3 grid(static_cast<unsigned>(parts), static_cast<unsigned>(kc.H),
             static_cast<unsigned>(q.B));
+  timing_begin(kKidDecode, s);
   switch (q.H / kc.H) {
     case 1: decode_partials_kernel<1><<<grid, 256, 0, s>>>(p); break;
     case 2: decode_partials_kernel<2><<<grid, 256, 0, s>>>(p); break;
@@ -201,6 +202,7 @@ int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
     case 8: decode_partials_kernel<8><<<grid, 256, 0, s>>>(p); break;
     default: return LSX_ERR_UNSUPPORTED;
   }
+  timing_end(kKidDecode, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 

@@ -491,7 +491,9 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
                            static_cast<int>(smem)) != cudaSuccess)
     return LSX_ERR_LAUNCH;
   const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+  timing_begin(kKidFwdTc, s);
   fwd_tc_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, p);
+  timing_end(kKidFwdTc, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 

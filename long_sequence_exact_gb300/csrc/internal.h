@@ -19,6 +19,15 @@ struct DeviceCtx {
 // Fills ctx for the current device; returns LSX_OK or LSX_ERR_DEVICE.
 int device_ctx(DeviceCtx* ctx);
 
+// Optional per-kernel timing (lsx_timing_enable): a CUDA event pair is
+// recorded on the launching stream around every launch of kernel `kid`.
+enum KernelId {
+  kKidFwdTc = 0, kKidDkdv, kKidDq, kKidRowDot, kKidMerge, kKidTreeMerge,
+  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidCount
+};
+void timing_begin(int kid, cudaStream_t s);
+void timing_end(int kid, cudaStream_t s);
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Element offset of (b, h, n, 0) in a view.

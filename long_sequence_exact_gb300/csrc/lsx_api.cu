@@ -32,7 +32,52 @@ struct DevCache {
 std::mutex g_mu;
 std::vector<DevCache> g_devs;
 
+// ------------------------------------------------------- kernel timing
+const char* const kKernelNames[kKidCount] = {
+    "fwd_tc", "bwd_dkdv_tc", "bwd_dq_tc", "bwd_row_dot", "merge", "tree_merge",
+    "decode_partials", "simt_fwd", "simt_bwd", "fill"};
+std::atomic<bool> g_timing{false};
+struct TimedLaunch {
+  int kid;
+  cudaEvent_t a, b;
+};
+std::vector<TimedLaunch> g_launches;   // guarded by g_tmu
+std::vector<cudaEvent_t> g_event_pool; // guarded by g_tmu
+std::mutex g_tmu;
+int g_open_kid = -1;
+cudaEvent_t g_open_ev = nullptr;
+
+cudaEvent_t pooled_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+
 }  // namespace
+
+void timing_begin(int kid, cudaStream_t s) {
+  if (!g_timing.load()) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  g_open_kid = kid;
+  g_open_ev = pooled_event();
+  cudaEventRecord(g_open_ev, s);
+}
+
+void timing_end(int kid, cudaStream_t s) {
+  if (!g_timing.load()) return;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  if (g_open_kid != kid || g_open_ev == nullptr) return;
+  cudaEvent_t e = pooled_event();
+  cudaEventRecord(e, s);
+  g_launches.push_back({kid, g_open_ev, e});
+  g_open_kid = -1;
+  g_open_ev = nullptr;
+}
 
 int device_ctx(DeviceCtx* ctx) {
   int dev = 0;
@@ -399,6 +444,48 @@ int attn_decode(const lsx_tensor* q, const lsx_tensor* kc,
   lsx_tensor pl{part_l, LSX_F32, 0, q->B, q->H, 1, 1, q->H, 1, 1};
   return launch_tree_merge(po, rows * q->D, pl, rows, static_cast<int>(parts), *o,
                            *lse, ctx, s);
+}
+
+// ----------------------------------------------------------------- timing
+int lsx_timing_enable(int on) {
+  g_timing.store(on != 0);
+  return LSX_OK;
+}
+
+int lsx_timing_reset(void) {
+  std::lock_guard<std::mutex> lk(g_tmu);
+  for (auto& t : g_launches) {
+    g_event_pool.push_back(t.a);
+    g_event_pool.push_back(t.b);
+  }
+  g_launches.clear();
+  return LSX_OK;
+}
+
+int lsx_timing_report(char* buf, size_t n) {
+  if (buf == nullptr || n == 0) return LSX_ERR_NULL;
+  std::lock_guard<std::mutex> lk(g_tmu);
+  double total[kKidCount] = {0};
+  int64_t count[kKidCount] = {0};
+  for (auto& t : g_launches) {
+    if (cudaEventSynchronize(t.b) != cudaSuccess) return LSX_ERR_LAUNCH;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, t.a, t.b) != cudaSuccess) return LSX_ERR_LAUNCH;
+    total[t.kid] += ms;
+    count[t.kid] += 1;
+  }
+  size_t used = 0;
+  int reported = 0;
+  buf[0] = '\0';
+  for (int k = 0; k < kKidCount; ++k) {
+    if (count[k] == 0) continue;
+    const int w = snprintf(buf + used, n - used, "%s %lld %.6f\n", kKernelNames[k],
+                           static_cast<long long>(count[k]), total[k]);
+    if (w < 0 || static_cast<size_t>(w) >= n - used) break;
+    used += static_cast<size_t>(w);
+    ++reported;
+  }
+  return reported;
 }
 
 // ------------------------------------------------------------ diagnostics

@@ -307,7 +307,9 @@ int launch_merge(const lsx_tensor& oa, const lsx_tensor& la,
   const int64_t rows = oa.B * oa.H * oa.N;
   if (rows == 0) return LSX_OK;
   const int grid = grid_for_rows(rows, ctx, 8);
+  timing_begin(kKidMerge, s);
   LSX_DISPATCH_E(oa.D, merge_kernel<E><<<grid, 256, 0, s>>>(oa, la, ob, lb, oo, lo, rows));
+  timing_end(kKidMerge, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 
@@ -317,6 +319,7 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
                       cudaStream_t s) {
   const int64_t rows = op.B * op.H * op.N;
   if (rows == 0) return LSX_OK;
+  timing_begin(kKidTreeMerge, s);
   if (n_parts <= 16) {
     const int grid = grid_for_rows(rows, ctx, 8);
     LSX_DISPATCH_E(op.D, tree_merge_warp_kernel<E><<<grid, 256, 0, s>>>(
@@ -327,6 +330,7 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
     LSX_DISPATCH_E(op.D, tree_merge_block_kernel<E><<<grid, 256, 0, s>>>(
                              op, pso, lp, psl, n_parts, oo, lo, rows));
   }
+  timing_end(kKidTreeMerge, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 
@@ -335,7 +339,9 @@ int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
   const int64_t rows = o.B * o.H * o.N;
   if (rows == 0) return LSX_OK;
   const int grid = grid_for_rows(rows, ctx, 8);
+  timing_begin(kKidRowDot, s);
   LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid, 256, 0, s>>>(o, d_o, delta, rows));
+  timing_end(kKidRowDot, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 
@@ -344,7 +350,9 @@ int launch_fill_empty(const lsx_tensor& o, const lsx_tensor& lse,
   const int64_t rows = o.B * o.H * o.N;
   if (rows == 0) return LSX_OK;
   const int grid = grid_for_rows(rows, ctx, 8);
+  timing_begin(kKidFill, s);
   LSX_DISPATCH_E(o.D, fill_kernel<E><<<grid, 256, 0, s>>>(o, lse, rows));
+  timing_end(kKidFill, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 

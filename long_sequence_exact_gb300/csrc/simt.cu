@@ -245,12 +245,14 @@ int launch_simt_fwd(const lsx_tensor& q, const lsx_tensor& k,
   if (rows == 0) return LSX_OK;
   const PairGeom g{q_off, kv_off, causal};
   const int grid = grid_rows(rows, ctx);
+  timing_begin(kKidSimtFwd, s);
   if (q.D == 128)
     simt_fwd_kernel<4><<<grid, 256, 0, s>>>(q, k, v, o, lse, g, scale, accumulate);
   else if (q.D == 64)
     simt_fwd_kernel<2><<<grid, 256, 0, s>>>(q, k, v, o, lse, g, scale, accumulate);
   else
     return LSX_ERR_UNSUPPORTED;
+  timing_end(kKidSimtFwd, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 
@@ -264,6 +266,7 @@ int launch_simt_bwd(const lsx_tensor& q, const lsx_tensor& k,
   const PairGeom g{q_off, kv_off, causal};
   const int64_t qrows = q.B * q.H * q.N, krows = k.B * k.H * k.N;
   if (q.D != 128 && q.D != 64) return LSX_ERR_UNSUPPORTED;
+  timing_begin(kKidSimtBwd, s);
   if (qrows > 0) {
     const int grid = grid_rows(qrows, ctx);
     if (q.D == 128)
@@ -278,6 +281,7 @@ int launch_simt_bwd(const lsx_tensor& q, const lsx_tensor& k,
     else
       simt_dkdv_kernel<2><<<grid, 256, 0, s>>>(q, k, v, lse, d_o, delta, dk, dv, g, scale, accumulate);
   }
+  timing_end(kKidSimtBwd, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 

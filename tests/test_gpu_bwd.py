@@ -1,0 +1,89 @@
+"""tcgen05 backward (bf16) against the fp64 oracle's explicit-Jacobian
+backward, through the C ABI."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+import long_sequence_exact_gb300 as lsx
+from long_sequence_exact_gb300.inputs import random_tensor
+from helpers import TOL_GRAD_REL, f64, rel_fro
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def make(b, hq, hkv, lq, lk, d, seed, amp=1.0):
+    q = random_tensor((b, hq, lq, d), seed, amp, device=DEV)
+    k = random_tensor((b, hkv, lk, d), seed + 1, amp, device=DEV)
+    v = random_tensor((b, hkv, lk, d), seed + 2, device=DEV)
+    d_o = random_tensor((b, hq, lq, d), seed + 3, device=DEV)
+    return q, k, v, d_o
+
+
+def check_grads(got, ref, tol=TOL_GRAD_REL):
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        gg = f64(g)
+        assert not np.any(np.isnan(gg)), f"{name} has NaN"
+        e = rel_fro(gg, r)
+        assert e <= tol, f"{name} relative Frobenius error {e:.3e} > {tol}"
+
+
+CASES = [
+    # B, Hq, Hkv, Lq, Lk, D, q_off, kv_off, causal
+    (1, 2, 2, 256, 256, 128, 0, 0, True),
+    (1, 2, 2, 256, 256, 128, 0, 0, False),
+    (1, 2, 2, 256, 256, 64, 0, 0, True),
+    (2, 4, 2, 200, 333, 128, 0, 0, False),   # ragged tails, GQA
+    (1, 2, 2, 384, 384, 64, 0, 0, True),
+    (1, 2, 2, 300, 500, 128, 200, 0, True),  # causal with offsets
+    (1, 3, 1, 130, 700, 128, 1000, 600, True),
+    (1, 2, 2, 128, 256, 128, 0, 64, True),   # rows and keys nobody pairs
+    (1, 1, 1, 1000, 1000, 128, 0, 0, True),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
+def test_chunk_bwd_matches_oracle(case, grad_dtype):
+    b, hq, hkv, lq, lk, d, q_off, kv_off, causal = case
+    q, k, v, d_o = make(b, hq, hkv, lq, lk, d, seed=lq + 7 * lk)
+    # the saved O and LSE come from the GPU forward (as in training)
+    o, lse = lsx.chunk_fwd(q, k, v, q_off, kv_off, causal)
+    grads = lsx.chunk_bwd(q, k, v, o, lse, d_o, q_off, kv_off, causal, grad_dtype=grad_dtype)
+    torch.cuda.synchronize()
+    assert lsx.sync_status() == 0
+    ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), q_off, kv_off, causal)
+    check_grads(grads, ref)
+
+
+def test_chunked_bwd_over_chunk_pairs_accumulates():
+    # two query chunks x two key chunks, causal, f32 accumulation across pairs
+    n, c = 1024, 512
+    q, k, v, d_o = make(1, 4, 4, n, n, 128, seed=3, amp=0.5)
+    o, lse = lsx.chunked_fwd(q, k, v, chunk_len=c, causal=True)
+    dq = torch.zeros(q.shape, dtype=torch.float32, device=DEV)
+    dk = torch.zeros(k.shape, dtype=torch.float32, device=DEV)
+    dv = torch.zeros(v.shape, dtype=torch.float32, device=DEV)
+    for qc in range(2):
+        qs = slice(qc * c, (qc + 1) * c)
+        for kc in range(qc + 1):
+            ks = slice(kc * c, (kc + 1) * c)
+            lsx.chunk_bwd(q[:, :, qs], k[:, :, ks], v[:, :, ks], o[:, :, qs], lse[:, :, qs],
+                          d_o[:, :, qs], qc * c, kc * c, True, dq=dq[:, :, qs],
+                          dk=dk[:, :, ks], dv=dv[:, :, ks], accumulate=True)
+    ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), 0, 0, True)
+    check_grads((dq, dk, dv), ref)
+    # the whole-sequence call gives the same gradients
+    g2 = lsx.chunked_bwd(q, k, v, o, lse, d_o, chunk_len=c, causal=True)
+    check_grads(g2, ref)
+
+
+def test_backward_is_deterministic():
+    q, k, v, d_o = make(1, 4, 4, 768, 768, 128, seed=5)
+    o, lse = lsx.chunk_fwd(q, k, v, 0, 0, True)
+    a = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
+    b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
