@@ -135,6 +135,10 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = WORKLOADS[WORKLOAD]
+    workload = WORKLOAD
+    if args.n or args.heads:
+        w = w.with_(N=args.n or w.N, Hq=args.heads or w.Hq, Hkv=args.heads or w.Hkv)
+        workload = f"causal_{w.N}_h{w.Hq}_profiling"
     x = make_inputs(w, device=dev, seed=w.seed + rank)
     q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
     o = torch.empty_like(q)
@@ -267,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*0.5 q/k/v, N(0,1) dO; one problem per rank)",
-        "config": {"workload": WORKLOAD, "B": w.B, "H": w.Hq, "N": w.N, "d": w.D,
+        "config": {"workload": workload, "B": w.B, "H": w.Hq, "N": w.N, "d": w.D,
                    "chunk_len": w.chunk, "causal": True,
                    "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd,
                    "l2": "inputs larger than L2 (q, k, v, dO 1 GiB each; no flush needed)",
@@ -345,6 +349,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
+    ap.add_argument("--n", type=int, default=None,
+                    help="sequence length override (profiling captures on a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="head count override (profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
