@@ -155,6 +155,36 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
                    size_t workspace_bytes, lsx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * attn_chunk_bwd_noalloc -- attn_chunk_bwd for callers that cannot allocate
+ * device memory when they call it (the paper has no counterpart; this is a
+ * deployment convenience of the library).  Examples: an extension running
+ * inside a host application that owns the device memory pool and offers no
+ * way to request more, or a latency-critical loop that forbids allocation
+ * after start-up.  Same tensors, semantics and results as attn_chunk_bwd,
+ * but no workspace argument: the row dot products go to a fixed 16 MiB array
+ * compiled into the library (attn_chunk_bwd_noalloc_max_bytes()), which every
+ * GPU that loads the library holds until the process exits.
+ *  - Limit: attn_chunk_bwd_workspace_size(q, k) must not exceed that size
+ *    (B * Hq * Lq <= 4,194,304 query rows); larger problems return
+ *    LSX_ERR_WORKSPACE and launch nothing.
+ *  - The array is shared by every call on a device and keeps the last
+ *    call's contents (nothing in it needs to start at zero).  Calls whose
+ *    work overlaps on the GPU race on it: order them on one stream.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress) and caches it; make that
+ *    first call before any stream capture.
+ *  - Allocates nothing (no cudaMalloc / cudaFree / allocating library call).
+ * ---------------------------------------------------------------------- */
+size_t attn_chunk_bwd_noalloc_max_bytes(void);
+int attn_chunk_bwd_noalloc(const lsx_tensor* q, const lsx_tensor* k,
+                           const lsx_tensor* v, const lsx_tensor* o,
+                           const lsx_tensor* lse, const lsx_tensor* d_o,
+                           int64_t q_off, int64_t kv_off, int causal,
+                           float scale, const lsx_tensor* dq,
+                           const lsx_tensor* dk, const lsx_tensor* dv,
+                           int accumulate, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * attn_chunked_fwd / attn_chunked_bwd -- a whole sequence [B, H, N, D] split
  * into chunks of chunk_len rows, every (query chunk, key chunk) pair that the
  * mask leaves visible computed in ONE persistent launch whose CTAs take

@@ -58,6 +58,9 @@ SIGNATURES = {
     "attn_chunk_bwd_workspace_size": (_SZ, [_P, _P]),
     "attn_chunk_bwd": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _INT, ctypes.c_float,
                               _P, _P, _P, _INT, _VP, _SZ, _VP]),
+    "attn_chunk_bwd_noalloc_max_bytes": (_SZ, []),
+    "attn_chunk_bwd_noalloc": (_INT, [_P, _P, _P, _P, _P, _P, _I64, _I64, _INT, ctypes.c_float,
+                                      _P, _P, _P, _INT, _VP]),
     "attn_chunked_fwd_workspace_size": (_SZ, [_P, _P, _I64, _INT]),
     "attn_chunked_fwd": (_INT, [_P, _P, _P, _I64, _INT, ctypes.c_float, _P, _P, _VP, _SZ, _VP]),
     "attn_chunked_bwd_workspace_size": (_SZ, [_P, _P, _I64, _INT]),
