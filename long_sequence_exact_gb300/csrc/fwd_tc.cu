@@ -28,9 +28,12 @@
 //   warps 8..11   softmax of query tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [384,384+D);
 // P_t (bf16 pairs) overwrites the first 64 columns of S_t after the softmax
-// has read S_t, and S_t is only re-issued once the P_t V product completed.
-// The two query tiles ping-pong: the tensor pipe computes one tile's
-// products while the other tile's softmax runs on the CUDA cores.
+// has read S_t.  The MMA issue order per key tile j is
+//   P_0 V_j, S_0(j+1), P_1 V_j, S_1(j+1)
+// so each tile's softmax overlaps two MMAs of the other tile.  K and V slots
+// are released separately (K after the S products, V after the P V ones).
+// Softmax: all four TMEM loads in flight at once, 3-input max, packed fp32
+// FMA/add (two elements per instruction) for the exp2 argument and row sum.
 //
 // Rescaling: the output is rescaled only when the row maximum grows by more
 // than 8 (base 2); otherwise the stale maximum is kept, so exp2 arguments
@@ -66,7 +69,8 @@ struct __align__(1024) FwdSmem {
   uint64_t q_full, q_empty, final_bar;
   uint64_t k_full[FwdCfg<D>::kStages];
   uint64_t v_full[FwdCfg<D>::kStages];
-  uint64_t kv_empty[FwdCfg<D>::kStages];
+  uint64_t k_empty[FwdCfg<D>::kStages];
+  uint64_t v_empty[FwdCfg<D>::kStages];
   uint64_t s_full[2], p_full[2], o_full[2];
   uint32_t tmem_base;
   int abort;
@@ -137,7 +141,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.k_full[s], 1);
       mbar_init(&sm.v_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.k_empty[s], 1);
+      mbar_init(&sm.v_empty[s], 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&sm.s_full[t], 1);
@@ -160,10 +165,10 @@ __global__ void __launch_bounds__(384, 1)
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
   // 384 threads launched at <= 168 registers (64,512).  Producer/MMA
-  // warpgroup keeps 64, the two softmax warpgroups take 216:
-  // 128 * 64 + 256 * 216 = 63,488 <= 64,512.
+  // warpgroup keeps 80, the two softmax warpgroups take 208:
+  // 128 * 80 + 256 * 208 = 63,488 <= 64,512.
   if (warp < 4) {
-  regs_dec<64>();
+  regs_dec<80>();
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0, qe_phase = 0;
@@ -182,12 +187,13 @@ __global__ void __launch_bounds__(384, 1)
                       static_cast<int>(x.h), static_cast<int>(x.b));
       bool ok = true;
       for (int64_t j = 0; j < nkv; ++j) {
-        if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
+        if (!mbar_wait(&sm.k_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.k_full[stage], Cfg::kTileBytes);
         for (int sub = 0; sub < Cfg::kSub; ++sub)
           tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.k_full[stage],
                       sub * 64, static_cast<int>(j * 128),
                       static_cast<int>(x.hk), static_cast<int>(x.b));
+        if (!mbar_wait(&sm.v_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.v_full[stage], Cfg::kTileBytes);
         for (int sub = 0; sub < Cfg::kSub; ++sub)
           tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.v_full[stage],
@@ -201,11 +207,26 @@ __global__ void __launch_bounds__(384, 1)
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
     constexpr uint32_t kIdO = idesc_bf16_f32(128, D, 0, 1);
-    uint32_t stage = 0, phase = 0, q_phase = 0;
-    uint32_t p_phase[2] = {0, 0}, o_phase[2] = {0, 0};
-    bool o_pending[2] = {false, false};
+    // Order per key tile j:  P_0 V_j, S_0 = Q_0 K_{j+1}^T, P_1 V_j, S_1 = ...
+    // S_t(j+1) overwrites the TMEM columns that P_t(j) occupies; it is
+    // issued right after P_t(j) V_j by this same thread, and one thread's
+    // tcgen05.mma operations execute in issue order, so the P_t(j) reads of
+    // the earlier MMA precede the S_t(j+1) writes of the later one.  This
+    // gives each tile's softmax the time of two other MMAs (P_{1-t} V and
+    // S_{1-t}) to finish before its P_t V is due.
+    uint32_t kst = 0, kph = 0, vst = 0, vph = 0, q_phase = 0;
+    uint32_t p_phase[2] = {0, 0};
     bool issued = false;
     const uint32_t q_addr[2] = {smem_addr(sm.q[0]), smem_addr(sm.q[1])};
+    auto issue_s = [&](int t, uint32_t k_addr) {
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+        mma_ss(tmem + t * 128, sdesc_sw128(q_addr[t] + off, 16, 1024),
+               sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+      }
+      mma_commit(&sm.s_full[t]);
+    };
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
@@ -215,48 +236,53 @@ __global__ void __launch_bounds__(384, 1)
       q_phase ^= 1;
       tc_fence_after();
       bool ok = true;
-      for (int64_t j = 0; j < nkv && ok; ++j) {
-        if (!mbar_wait(&sm.k_full[stage], phase, guard)) { ok = false; break; }
+      if (nkv > 0) {  // S_t(0)
+        if (!mbar_wait(&sm.k_full[kst], kph, guard)) break;
         tc_fence_after();
-        const uint32_t k_addr = smem_addr(sm.k[stage]);
+        for (int t = 0; t < 2; ++t)
+          if (x.nkv[t] > 0) issue_s(t, smem_addr(sm.k[kst]));
+        issued = true;
+        mma_commit(&sm.k_empty[kst]);
+        if (++kst == kStages) { kst = 0; kph ^= 1; }
+      }
+      for (int64_t j = 0; j < nkv; ++j) {
+        if (!mbar_wait(&sm.v_full[vst], vph, guard)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t v_addr = smem_addr(sm.v[vst]);
+        const bool has_next = j + 1 < nkv;
+        bool k_ready = false;
         for (int t = 0; t < 2; ++t) {
-          if (j >= x.nkv[t]) continue;
-          if (o_pending[t]) {  // P_t aliases S_t: wait for the last P_t V
-            if (!mbar_wait(&sm.o_full[t], o_phase[t], guard)) { ok = false; break; }
-            o_phase[t] ^= 1;
-            o_pending[t] = false;
+          if (j < x.nkv[t]) {
+            if (!mbar_wait(&sm.p_full[t], p_phase[t], guard)) { ok = false; break; }
+            p_phase[t] ^= 1;
             tc_fence_after();
-          }
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tmem + t * 128, sdesc_sw128(q_addr[t] + off, 16, 1024),
-                   sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+            for (int kk = 0; kk < 8; ++kk) {
+              mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                     sdesc_sw128(v_addr + kk * 2048, 128 * 128, 1024), kIdO,
+                     (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&sm.o_full[t]);
           }
-          mma_commit(&sm.s_full[t]);
-          issued = true;
+          if (has_next && j + 1 < x.nkv[t]) {
+            if (!k_ready) {
+              if (!mbar_wait(&sm.k_full[kst], kph, guard)) { ok = false; break; }
+              tc_fence_after();
+              k_ready = true;
+            }
+            issue_s(t, smem_addr(sm.k[kst]));
+          }
         }
         if (!ok) break;
-        if (!mbar_wait(&sm.v_full[stage], phase, guard)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t v_addr = smem_addr(sm.v[stage]);
-        for (int t = 0; t < 2; ++t) {
-          if (j >= x.nkv[t]) continue;
-          if (!mbar_wait(&sm.p_full[t], p_phase[t], guard)) { ok = false; break; }
-          p_phase[t] ^= 1;
-          tc_fence_after();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                   sdesc_sw128(v_addr + kk * 2048, 128 * 128, 1024), kIdO,
-                   (j > 0 || kk > 0) ? 1u : 0u);
+        if (has_next) {
+          if (!k_ready) {  // K_{j+1} unused by both tiles: still consume its slot
+            if (!mbar_wait(&sm.k_full[kst], kph, guard)) { ok = false; break; }
           }
-          mma_commit(&sm.o_full[t]);
-          o_pending[t] = true;
+          mma_commit(&sm.k_empty[kst]);
+          if (++kst == kStages) { kst = 0; kph ^= 1; }
         }
-        if (!ok) break;
-        mma_commit(&sm.kv_empty[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        mma_commit(&sm.v_empty[vst]);
+        if (++vst == kStages) { vst = 0; vph ^= 1; }
       }
       if (!ok) break;
       mma_commit(&sm.q_empty);
@@ -267,7 +293,7 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
   } else {
-    regs_inc<216>();
+    regs_inc<208>();
     // ------------------------------------------------------------- softmax
     const int t = (warp - 4) >> 2;
     const int row = threadIdx.x - 128 * (1 + t);  // 0..127 == TMEM lane
@@ -290,13 +316,24 @@ __global__ void __launch_bounds__(384, 1)
         s_phase ^= 1;
         tc_fence_after();
         float s[128];
+        {
+          // all four loads in flight before the single wait
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          tmem_ld32(tS, u0);
+          tmem_ld32(tS + 32, u1);
+          tmem_ld32(tS + 64, u2);
+          tmem_ld32(tS + 96, u3);
+          tmem_ld_wait32(u0);
+          reg_fence32(u1);
+          reg_fence32(u2);
+          reg_fence32(u3);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[32];
-          tmem_ld32(tS + cc * 32, u);
-          tmem_ld_wait32(u);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(u[i]);
+          for (int i = 0; i < 32; ++i) {
+            s[i] = __uint_as_float(u0[i]);
+            s[32 + i] = __uint_as_float(u1[i]);
+            s[64 + i] = __uint_as_float(u2[i]);
+            s[96 + i] = __uint_as_float(u3[i]);
+          }
         }
         const int64_t kb = j * 128;
         const bool need_mask =
@@ -315,13 +352,13 @@ __global__ void __launch_bounds__(384, 1)
         }
         float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-        for (int i = 4; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, s[i]);
-          mx1 = fmaxf(mx1, s[i + 1]);
-          mx2 = fmaxf(mx2, s[i + 2]);
-          mx3 = fmaxf(mx3, s[i + 3]);
+        for (int i = 4; i < 128; i += 8) {
+          mx0 = fmax3(mx0, s[i], s[i + 1]);
+          mx1 = fmax3(mx1, s[i + 2], s[i + 3]);
+          mx2 = fmax3(mx2, s[i + 4], s[i + 5]);
+          mx3 = fmax3(mx3, s[i + 6], s[i + 7]);
         }
-        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+        const float mx = fmax3(fmaxf(mx0, mx1), mx2, mx3);
         const float m_new = fmaxf(m, mx * sl2);
         if (j == 0) {
           m = m_new;
@@ -348,21 +385,24 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
         const float mu = (m == kNegInf) ? 0.f : m;
-        float l0 = 0.f, l1 = 0.f;
+        // exp2(s * scale log2e - m) two at a time (packed fp32 FMA / add)
+        const float2 sc2 = make_float2(sl2, sl2);
+        const float2 nm2 = make_float2(-mu, -mu);
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float a = ex2(fmaf(s[cc * 32 + 2 * i], sl2, -mu));
-            const float b2 = ex2(fmaf(s[cc * 32 + 2 * i + 1], sl2, -mu));
-            l0 += a;
-            l1 += b2;
-            pk[i] = pack_bf16(a, b2);
+            const float2 arg =
+                __ffma2_rn(make_float2(s[cc * 32 + 2 * i], s[cc * 32 + 2 * i + 1]), sc2, nm2);
+            const float2 e = make_float2(ex2(arg.x), ex2(arg.y));
+            if (i & 1) lb = __fadd2_rn(lb, e); else la = __fadd2_rn(la, e);
+            pk[i] = pack_bf16(e.x, e.y);
           }
           tmem_st16(tS + cc * 16, pk);
         }
-        l += l0 + l1;
+        l += (la.x + la.y) + (lb.x + lb.y);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full[t]);

@@ -233,6 +233,22 @@ LSX_DEV void tmem_ld_wait32(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Compiler-only fence: uses of r cannot move above an earlier
+// tmem_ld_wait32 (lets several loads share one wait).
+LSX_DEV void reg_fence32(uint32_t (&r)[32]) {
+  asm volatile(
+      ""
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]),
+        "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]),
+        "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+        "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+        "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+        "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
 // 32 lanes x 16 consecutive 32-bit columns store (same lane mapping).
 LSX_DEV void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
@@ -281,6 +297,12 @@ LSX_DEV float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// max of three (one instruction on sm_100+)
+LSX_DEV float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 LSX_DEV float lg2(float x) {
   float y;
