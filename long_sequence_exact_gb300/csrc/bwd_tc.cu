@@ -5,8 +5,8 @@
 //
 // With P_ij = exp(scale <q_i,k_j> - LSE_i), delta_i = <dO_i, O_i> (computed
 // beforehand by the row-dot kernel from the saved O) and
-// dS_ij = scale * P_ij (dO_i.v_j - delta_i):
-//   dV = P^T dO,   dK = dS^T Q,   dQ = dS K.
+// dS_ij = P_ij (dO_i.v_j - delta_i):
+//   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
 //
 // Two persistent kernels, both deterministic (every output tile is owned by
 // exactly one CTA; no atomics):
@@ -15,17 +15,26 @@
 //    of the group) that sees it:
 //      S^T  = K Q_i^T     (SS, K-major x K-major)      TMEM [0,128)
 //      dP^T = V dO_i^T    (SS)                         TMEM [128,256)
-//      grad warps: P^T, dS^T -> bf16 back into TMEM [0,64), [128,192)
+//      grad warps: P^T, dS^T -> bf16 back into TMEM (inside [0,128), [128,256))
 //      dV  += P^T dO_i    (TS, dO_i MN-major)          TMEM [256,256+D)
 //      dK  += dS^T Q_i    (TS, Q_i MN-major)           TMEM [384,384+D)
 //  * dq_kernel, query-tile-major: a work item is one 128-row query tile; it
 //    walks every visible key tile:
 //      S  = Q K_j^T, dP = dO V_j^T (SS)                TMEM [0,128), [128,256)
-//      grad warps: dS -> bf16 into TMEM [128,192)
+//      grad warps: dS -> bf16 into TMEM (inside [128,256))
 //      dQ += dS K_j       (TS, K_j MN-major)           TMEM [256,256+D)
-// Roles per CTA (256 threads): warp 0 loads (TMA), warp 1 owns TMEM and
-// issues the MMAs (lane 0), warps 4..7 compute P and dS (thread = TMEM lane)
-// and write the outputs.  Work items are dealt longest-first in snake order.
+// Roles per CTA (384 threads): warp 0 loads (TMA), warp 1 owns TMEM and
+// issues the MMAs (lane 0), warps 4..11 compute P and dS and write the
+// outputs.  Grad warp g covers TMEM lanes 32 (g % 4) .. +31 and the half
+// g / 4 of the 128 columns; each half packs its bf16 result into the first
+// 32 columns of its own 64, so the two warps sharing a lane range never
+// touch each other's columns, and the TS MMAs address each 16-wide K step
+// of the bf16 operand at packed_col(kk).
+// MMA issue order: the next step's S/dP products are issued right after the
+// current dV/dK (dQ) products without waiting for them; one thread's
+// tcgen05.mma operations execute in issue order, so the bf16 operands read
+// by the earlier MMAs are consumed before the later MMAs overwrite them.
+// Work items are dealt longest-first in snake order.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -64,6 +73,12 @@ struct BwdParams {
   uint64_t wait_ns;
 };
 
+// TMEM column (relative to the 128-column fp32 tile) of the packed bf16
+// operand for K step kk (16 elements = 8 packed columns).
+__device__ __forceinline__ uint32_t packed_col(int kk) {
+  return kk < 4 ? static_cast<uint32_t>(kk * 8) : static_cast<uint32_t>(64 + (kk - 4) * 8);
+}
+
 // First query tile that sees key tile j (n_qtiles when none does).
 __device__ __forceinline__ int64_t q_tile_begin(const BwdParams& p, int64_t j) {
   if (!p.causal) return 0;
@@ -81,10 +96,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
-// Row of D fp32 values (from TMEM, 32 at a time) scaled and written to a
-// bf16 or f32 output, optionally added to what is there.
+// 32 fp32 values scaled by `mult` and written to a bf16 or f32 output row,
+// optionally added to what is there.
 __device__ __forceinline__ void store_row32(void* out, int f32, int64_t off,
-                                            const float (&v)[32], int accumulate) {
+                                            const uint32_t (&u)[32], float mult,
+                                            int accumulate) {
+  float v[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(u[i]) * mult;
   if (f32) {
     float* dst = static_cast<float*>(out) + off;
 #pragma unroll
@@ -123,6 +142,20 @@ __device__ __forceinline__ void store_row32(void* out, int f32, int64_t off,
   }
 }
 
+// Loads 64 fp32 columns (two x32 loads) of two TMEM tiles with one wait.
+__device__ __forceinline__ void ld_two_halves(uint32_t ta, uint32_t tb, uint32_t (&a0)[32],
+                                              uint32_t (&a1)[32], uint32_t (&b0)[32],
+                                              uint32_t (&b1)[32]) {
+  tmem_ld32(ta, a0);
+  tmem_ld32(ta + 32, a1);
+  tmem_ld32(tb, b0);
+  tmem_ld32(tb + 32, b1);
+  tmem_ld_wait32(a0);
+  reg_fence32(a1);
+  reg_fence32(b0);
+  reg_fence32(b1);
+}
+
 // ===================================================================== dK dV
 template <int D>
 struct DkdvSmem {
@@ -158,7 +191,7 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v,
@@ -182,7 +215,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&sm.st_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.p_full, 256);
     mbar_init(&sm.dkv_done, 1);
     fence_barrier_init();
   }
@@ -196,129 +229,134 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
 
-  if (warp == 0) {
-    // ---------------------------------------------------- loads (warp 0)
-    uint32_t stage = 0, phase = 0, kv_phase = 0;
-    for (int64_t r = 0;; ++r) {
-      const int64_t it = snake_item(c, r, G);
-      if (it >= p.n_items) break;
-      const DkdvItem x = dkdv_item(p, it);
-      if (!mbar_wait(&sm.kv_empty, kv_phase ^ 1, guard)) break;
-      kv_phase ^= 1;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-        for (int sub = 0; sub < kSub; ++sub) {
-          tma_load_4d(&sm.k[sub * 128 * 64], &tm_k, &sm.kv_full, sub * 64,
-                      static_cast<int>(x.j * 128), static_cast<int>(x.hk),
-                      static_cast<int>(x.b));
-          tma_load_4d(&sm.v[sub * 128 * 64], &tm_v, &sm.kv_full, sub * 64,
-                      static_cast<int>(x.j * 128), static_cast<int>(x.hk),
-                      static_cast<int>(x.b));
-        }
-      }
-      bool ok = true;
-      for (int64_t s = 0; s < x.n_i; ++s) {
-        const int64_t h = x.hk * x.group + s / (p.n_qtiles - x.i0);
-        const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
-        if (!mbar_wait(&sm.st_empty[stage], phase ^ 1, guard)) { ok = false; break; }
-        // LSE (as log2 units) and delta of the 128 query rows of tile i
-        for (int t = lane; t < 128; t += 32) {
-          const int64_t row = i * 128 + t;
-          float l2 = kPosInf, dl = 0.f;
-          if (row < p.Lq) {
-            const float lse = p.lse[x.b * p.l_sb + h * p.l_sh + row * p.l_sn];
-            l2 = (lse == kNegInf) ? kPosInf : lse * kLog2e;
-            dl = p.delta[(x.b * p.Hq + h) * p.Lq + row];
-          }
-          sm.lse2[stage][t] = l2;
-          sm.delta[stage][t] = dl;
-        }
+  // 384 threads launched at <= 168 registers (64,512): the load/MMA
+  // warpgroup keeps 88, the two grad warpgroups take 184:
+  // 128 * 88 + 256 * 184 = 58,368 <= 64,512.
+  if (warp < 4) {
+    regs_dec<88>();
+    if (warp == 0) {
+      // -------------------------------------------------- loads (warp 0)
+      uint32_t stage = 0, phase = 0, kv_phase = 0;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DkdvItem x = dkdv_item(p, it);
+        if (!mbar_wait(&sm.kv_empty, kv_phase ^ 1, guard)) break;
+        kv_phase ^= 1;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&sm.st_full[stage], 2 * kTile);
+          mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
           for (int sub = 0; sub < kSub; ++sub) {
-            tma_load_4d(&sm.q[stage][sub * 128 * 64], &tm_q, &sm.st_full[stage], sub * 64,
-                        static_cast<int>(i * 128), static_cast<int>(h), static_cast<int>(x.b));
-            tma_load_4d(&sm.d_o[stage][sub * 128 * 64], &tm_do, &sm.st_full[stage], sub * 64,
-                        static_cast<int>(i * 128), static_cast<int>(h), static_cast<int>(x.b));
+            tma_load_4d(&sm.k[sub * 128 * 64], &tm_k, &sm.kv_full, sub * 64,
+                        static_cast<int>(x.j * 128), static_cast<int>(x.hk),
+                        static_cast<int>(x.b));
+            tma_load_4d(&sm.v[sub * 128 * 64], &tm_v, &sm.kv_full, sub * 64,
+                        static_cast<int>(x.j * 128), static_cast<int>(x.hk),
+                        static_cast<int>(x.b));
           }
-        } else {
-          mbar_arrive(&sm.st_full[stage]);
         }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        bool ok = true;
+        for (int64_t s = 0; s < x.n_i; ++s) {
+          const int64_t h = x.hk * x.group + s / (p.n_qtiles - x.i0);
+          const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
+          if (!mbar_wait(&sm.st_empty[stage], phase ^ 1, guard)) { ok = false; break; }
+          // LSE (as log2 units) and delta of the 128 query rows of tile i
+          for (int t = lane; t < 128; t += 32) {
+            const int64_t row = i * 128 + t;
+            float l2 = kPosInf, dl = 0.f;
+            if (row < p.Lq) {
+              const float lse = p.lse[x.b * p.l_sb + h * p.l_sh + row * p.l_sn];
+              l2 = (lse == kNegInf) ? kPosInf : lse * kLog2e;
+              dl = p.delta[(x.b * p.Hq + h) * p.Lq + row];
+            }
+            sm.lse2[stage][t] = l2;
+            sm.delta[stage][t] = dl;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.st_full[stage], 2 * kTile);
+            for (int sub = 0; sub < kSub; ++sub) {
+              tma_load_4d(&sm.q[stage][sub * 128 * 64], &tm_q, &sm.st_full[stage], sub * 64,
+                          static_cast<int>(i * 128), static_cast<int>(h), static_cast<int>(x.b));
+              tma_load_4d(&sm.d_o[stage][sub * 128 * 64], &tm_do, &sm.st_full[stage],
+                          sub * 64, static_cast<int>(i * 128), static_cast<int>(h),
+                          static_cast<int>(x.b));
+            }
+          } else {
+            mbar_arrive(&sm.st_full[stage]);
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
-      if (!ok) break;
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ------------------------------------------------------------- MMA issue
-    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
-    uint32_t stage = 0, phase = 0, kv_phase = 0, p_phase = 0, d_phase = 0;
-    bool d_pending = false, issued = false;
-    const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
-    for (int64_t r = 0;; ++r) {
-      const int64_t it = snake_item(c, r, G);
-      if (it >= p.n_items) break;
-      const DkdvItem x = dkdv_item(p, it);
-      if (!mbar_wait(&sm.kv_full, kv_phase, guard)) break;
-      kv_phase ^= 1;
-      tc_fence_after();
-      bool ok = true;
-      for (int64_t s = 0; s < x.n_i; ++s) {
-        if (!mbar_wait(&sm.st_full[stage], phase, guard)) { ok = false; break; }
+    } else if (warp == 1 && lane == 0) {
+      // ----------------------------------------------------------- MMA issue
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
+      uint32_t stage = 0, phase = 0, kv_phase = 0, p_phase = 0;
+      bool issued = false;
+      const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DkdvItem x = dkdv_item(p, it);
+        if (!mbar_wait(&sm.kv_full, kv_phase, guard)) break;
+        kv_phase ^= 1;
         tc_fence_after();
-        if (d_pending) {  // P^T / dS^T of the previous step live in S^T / dP^T
-          if (!mbar_wait(&sm.dkv_done, d_phase, guard)) { ok = false; break; }
-          d_phase ^= 1;
-          d_pending = false;
+        bool ok = true;
+        for (int64_t s = 0; s < x.n_i; ++s) {
+          if (!mbar_wait(&sm.st_full[stage], phase, guard)) { ok = false; break; }
           tc_fence_after();
-        }
-        const uint32_t q_addr = smem_addr(sm.q[stage]);
-        const uint32_t o_addr = smem_addr(sm.d_o[stage]);
+          const uint32_t q_addr = smem_addr(sm.q[stage]);
+          const uint32_t o_addr = smem_addr(sm.d_o[stage]);
 #pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-          mma_ss(tmem + 0, sdesc_sw128(k_addr + off, 16, 1024),
-                 sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0);
-        }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tmem + 0, sdesc_sw128(k_addr + off, 16, 1024),
+                   sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0);
+          }
 #pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-          mma_ss(tmem + 128, sdesc_sw128(v_addr + off, 16, 1024),
-                 sdesc_sw128(o_addr + off, 16, 1024), kIdS, kk > 0);
-        }
-        mma_commit(&sm.s_full);
-        issued = true;
-        if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
-        p_phase ^= 1;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tmem + 128, sdesc_sw128(v_addr + off, 16, 1024),
+                   sdesc_sw128(o_addr + off, 16, 1024), kIdS, kk > 0);
+          }
+          mma_commit(&sm.s_full);
+          issued = true;
+          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
+          p_phase ^= 1;
+          tc_fence_after();
 #pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-          mma_ts(tmem + 256, tmem + 0 + kk * 8, sdesc_sw128(o_addr + kk * 2048, 128 * 128, 1024),
-                 kIdG, acc);
-          mma_ts(tmem + 384, tmem + 128 + kk * 8,
-                 sdesc_sw128(q_addr + kk * 2048, 128 * 128, 1024), kIdG, acc);
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
+            mma_ts(tmem + 256, tmem + packed_col(kk),
+                   sdesc_sw128(o_addr + kk * 2048, 128 * 128, 1024), kIdG, acc);
+            mma_ts(tmem + 384, tmem + 128 + packed_col(kk),
+                   sdesc_sw128(q_addr + kk * 2048, 128 * 128, 1024), kIdG, acc);
+          }
+          mma_commit(&sm.dkv_done);
+          mma_commit(&sm.st_empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        mma_commit(&sm.dkv_done);
-        d_pending = true;
-        mma_commit(&sm.st_empty[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (!ok) break;
+        mma_commit(&sm.kv_empty);
       }
-      if (!ok) break;
-      mma_commit(&sm.kv_empty);
+      if (issued) {
+        mma_commit(&sm.final_bar);
+        drain_wait(&sm.final_bar, 0, p.wait_ns);
+      }
     }
-    if (issued) {
-      mma_commit(&sm.final_bar);
-      drain_wait(&sm.final_bar, 0, p.wait_ns);
-    }
-  } else if (warp >= 4) {
+  } else {
+    regs_inc<184>();
     // -------------------------------------------- P^T, dS^T and the epilogue
-    const int row = threadIdx.x - 128;  // key row within the tile = TMEM lane
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128;
+    const int g = warp - 4;
+    const int quad = g & 3, half = g >> 2;
+    const int row = quad * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 64 * half;        // S^T / P^T
+    const uint32_t tP = tmem + lane_base + 128 + 64 * half;  // dP^T / dS^T
     uint32_t stage = 0, phase = 0, s_phase = 0;
     uint32_t d_count = 0;
-    const float sl2 = p.scale_log2, sc = p.scale;
+    const float sl2 = p.scale_log2;
+    const float2 sc2 = make_float2(sl2, sl2);
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
@@ -332,33 +370,43 @@ __global__ void __launch_bounds__(256, 1)
         // the stage's LSE/delta rows were published with st_full
         if (!mbar_wait(&sm.st_full[stage], phase, guard)) { ok = false; break; }
         tc_fence_after();
-        // query columns c with q_off + 128 i + c >= key_abs are visible
+        uint32_t us0[32], us1[32], ud0[32], ud1[32];
+        ld_two_halves(tS, tP, us0, us1, ud0, ud1);
+        // query columns c (of this half) with q_off + 128 i + 64 half + c >=
+        // key_abs are visible
         int cmin = 0;
         if (p.causal) {
-          const int64_t t = key_abs - (p.q_off + i * 128);
-          cmin = t <= 0 ? 0 : (t > 128 ? 128 : static_cast<int>(t));
+          const int64_t tt = key_abs - (p.q_off + i * 128 + 64 * half);
+          cmin = tt <= 0 ? 0 : (tt > 64 ? 64 : static_cast<int>(tt));
         }
-        const float* l2 = sm.lse2[stage];
-        const float* dl = sm.delta[stage];
+        const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[stage][64 * half]);
+        const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[stage][64 * half]);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t us[32], ud[32];
-          tmem_ld32(tS + cc * 32, us);
-          tmem_ld32(tP + cc * 32, ud);
-          tmem_ld_wait32(us);
-          tmem_ld_wait32(ud);
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t(&us)[32] = cc ? us1 : us0;
+          const uint32_t(&ud)[32] = cc ? ud1 : ud0;
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = cc * 32 + 2 * e;
-            float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), sl2, -l2[c0]));
-            float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), sl2, -l2[c0 + 1]));
-            if (c0 < cmin) p0 = 0.f;
-            if (c0 + 1 < cmin) p1 = 0.f;
-            const float d0 = sc * p0 * (__uint_as_float(ud[2 * e]) - dl[c0]);
-            const float d1 = sc * p1 * (__uint_as_float(ud[2 * e + 1]) - dl[c0 + 1]);
-            pk[e] = pack_bf16(p0, p1);
-            dk[e] = pack_bf16(d0, d1);
+          for (int e4 = 0; e4 < 8; ++e4) {
+            const float4 l4 = l2v[cc * 8 + e4];
+            const float4 d4 = dlv[cc * 8 + e4];
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int e = e4 * 2 + hh;  // pair index within the chunk
+              const int c0 = cc * 32 + 2 * e;
+              const float2 nl = hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+              const float2 nd = hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+              const float2 arg = __ffma2_rn(
+                  make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
+              float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+              if (c0 < cmin) pr.x = 0.f;
+              if (c0 + 1 < cmin) pr.y = 0.f;
+              const float2 dpm = __fadd2_rn(
+                  make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
+              const float2 ds = __fmul2_rn(pr, dpm);
+              pk[e] = pack_bf16(pr.x, pr.y);
+              dk[e] = pack_bf16(ds.x, ds.y);
+            }
           }
           tmem_st16(tS + cc * 16, pk);
           tmem_st16(tP + cc * 16, dk);
@@ -370,37 +418,31 @@ __global__ void __launch_bounds__(256, 1)
         if (++stage == DkdvSmem<D>::kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
-      // epilogue: dV and dK rows of this key tile
+      // epilogue: half 0 writes dV, half 1 writes dK (times scale)
       if (x.n_i > 0) {
         if (!mbar_wait(&sm.dkv_done, (d_count - 1) & 1, guard)) break;
         tc_fence_after();
       }
       const int64_t krow = x.j * 128 + row;
       const bool valid = krow < p.Lk;
+      const uint32_t base_col = half == 0 ? 256u : 384u;
 #pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t base_col = which == 0 ? 256u : 384u;
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t u[32];
+        if (x.n_i > 0) {
+          tmem_ld32(tmem + lane_base + base_col + cc * 32, u);
+          tmem_ld_wait32(u);
+        } else {
 #pragma unroll
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t u[32];
-          if (x.n_i > 0) {
-            tmem_ld32(tmem + lane_base + base_col + cc * 32, u);
-            tmem_ld_wait32(u);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = 0u;
-          }
-          if (!valid) continue;
-          float vals[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) vals[e] = __uint_as_float(u[e]);
-          if (which == 0)
-            store_row32(p.dv, p.dv_f32, x.b * p.dv_sb + x.hk * p.dv_sh + krow * p.dv_sn + cc * 32,
-                        vals, p.accumulate);
-          else
-            store_row32(p.dk, p.dk_f32, x.b * p.dk_sb + x.hk * p.dk_sh + krow * p.dk_sn + cc * 32,
-                        vals, p.accumulate);
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
+        if (!valid) continue;
+        if (half == 0)
+          store_row32(p.dv, p.dv_f32, x.b * p.dv_sb + x.hk * p.dv_sh + krow * p.dv_sn + cc * 32,
+                      u, 1.f, p.accumulate);
+        else
+          store_row32(p.dk, p.dk_f32, x.b * p.dk_sb + x.hk * p.dk_sh + krow * p.dk_sn + cc * 32,
+                      u, p.scale, p.accumulate);
       }
       tc_fence_before();
     }
@@ -446,7 +488,7 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int64_t it) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v,
@@ -470,7 +512,7 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&sm.kv_empty[s], 1);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.p_full, 256);
     mbar_init(&sm.dq_done, 1);
     fence_barrier_init();
   }
@@ -484,101 +526,103 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
 
-  if (warp == 0 && lane == 0) {
-    uint32_t stage = 0, phase = 0, qo_phase = 0;
-    for (int64_t r = 0;; ++r) {
-      const int64_t it = snake_item(c, r, G);
-      if (it >= p.n_items) break;
-      const DqItem x = dq_item(p, it);
-      if (!mbar_wait(&sm.qo_empty, qo_phase ^ 1, guard)) break;
-      qo_phase ^= 1;
-      mbar_arrive_expect_tx(&sm.qo_full, 2 * kTile);
-      for (int sub = 0; sub < kSub; ++sub) {
-        tma_load_4d(&sm.q[sub * 128 * 64], &tm_q, &sm.qo_full, sub * 64,
-                    static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
-        tma_load_4d(&sm.d_o[sub * 128 * 64], &tm_do, &sm.qo_full, sub * 64,
-                    static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
-      }
-      bool ok = true;
-      for (int64_t j = 0; j < x.nkv; ++j) {
-        if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
-        mbar_arrive_expect_tx(&sm.kv_full[stage], 2 * kTile);
+  // same register split as dkdv_kernel: 128 * 88 + 256 * 184 <= 384 * 168
+  if (warp < 4) {
+    regs_dec<88>();
+    if (warp == 0 && lane == 0) {
+      uint32_t stage = 0, phase = 0, qo_phase = 0;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DqItem x = dq_item(p, it);
+        if (!mbar_wait(&sm.qo_empty, qo_phase ^ 1, guard)) break;
+        qo_phase ^= 1;
+        mbar_arrive_expect_tx(&sm.qo_full, 2 * kTile);
         for (int sub = 0; sub < kSub; ++sub) {
-          tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.kv_full[stage], sub * 64,
-                      static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
-          tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.kv_full[stage], sub * 64,
-                      static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
+          tma_load_4d(&sm.q[sub * 128 * 64], &tm_q, &sm.qo_full, sub * 64,
+                      static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
+          tma_load_4d(&sm.d_o[sub * 128 * 64], &tm_do, &sm.qo_full, sub * 64,
+                      static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
         }
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        bool ok = true;
+        for (int64_t j = 0; j < x.nkv; ++j) {
+          if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
+          mbar_arrive_expect_tx(&sm.kv_full[stage], 2 * kTile);
+          for (int sub = 0; sub < kSub; ++sub) {
+            tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.kv_full[stage], sub * 64,
+                        static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
+            tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.kv_full[stage], sub * 64,
+                        static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
+          }
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
       }
-      if (!ok) break;
-    }
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
-    uint32_t stage = 0, phase = 0, qo_phase = 0, p_phase = 0, d_phase = 0;
-    bool d_pending = false, issued = false;
-    const uint32_t q_addr = smem_addr(sm.q), o_addr = smem_addr(sm.d_o);
-    for (int64_t r = 0;; ++r) {
-      const int64_t it = snake_item(c, r, G);
-      if (it >= p.n_items) break;
-      const DqItem x = dq_item(p, it);
-      if (!mbar_wait(&sm.qo_full, qo_phase, guard)) break;
-      qo_phase ^= 1;
-      tc_fence_after();
-      bool ok = true;
-      for (int64_t j = 0; j < x.nkv; ++j) {
-        if (!mbar_wait(&sm.kv_full[stage], phase, guard)) { ok = false; break; }
+    } else if (warp == 1 && lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
+      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
+      uint32_t stage = 0, phase = 0, qo_phase = 0, p_phase = 0;
+      bool issued = false;
+      const uint32_t q_addr = smem_addr(sm.q), o_addr = smem_addr(sm.d_o);
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DqItem x = dq_item(p, it);
+        if (!mbar_wait(&sm.qo_full, qo_phase, guard)) break;
+        qo_phase ^= 1;
         tc_fence_after();
-        const uint32_t k_addr = smem_addr(sm.k[stage]);
-        const uint32_t v_addr = smem_addr(sm.v[stage]);
-#pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-          mma_ss(tmem + 0, sdesc_sw128(q_addr + off, 16, 1024),
-                 sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
-        }
-        if (d_pending) {  // dS of the previous key tile lives in the dP columns
-          if (!mbar_wait(&sm.dq_done, d_phase, guard)) { ok = false; break; }
-          d_phase ^= 1;
-          d_pending = false;
+        bool ok = true;
+        for (int64_t j = 0; j < x.nkv; ++j) {
+          if (!mbar_wait(&sm.kv_full[stage], phase, guard)) { ok = false; break; }
           tc_fence_after();
-        }
+          const uint32_t k_addr = smem_addr(sm.k[stage]);
+          const uint32_t v_addr = smem_addr(sm.v[stage]);
 #pragma unroll 1
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-          mma_ss(tmem + 128, sdesc_sw128(o_addr + off, 16, 1024),
-                 sdesc_sw128(v_addr + off, 16, 1024), kIdS, kk > 0);
-        }
-        mma_commit(&sm.s_full);
-        issued = true;
-        if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
-        p_phase ^= 1;
-        tc_fence_after();
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tmem + 0, sdesc_sw128(q_addr + off, 16, 1024),
+                   sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+          }
 #pragma unroll 1
-        for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tmem + 256, tmem + 128 + kk * 8,
-                 sdesc_sw128(k_addr + kk * 2048, 128 * 128, 1024), kIdG,
-                 (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(tmem + 128, sdesc_sw128(o_addr + off, 16, 1024),
+                   sdesc_sw128(v_addr + off, 16, 1024), kIdS, kk > 0);
+          }
+          mma_commit(&sm.s_full);
+          issued = true;
+          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
+          p_phase ^= 1;
+          tc_fence_after();
+#pragma unroll 1
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_ts(tmem + 256, tmem + 128 + packed_col(kk),
+                   sdesc_sw128(k_addr + kk * 2048, 128 * 128, 1024), kIdG,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&sm.dq_done);
+          mma_commit(&sm.kv_empty[stage]);
+          if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
-        mma_commit(&sm.dq_done);
-        d_pending = true;
-        mma_commit(&sm.kv_empty[stage]);
-        if (++stage == kStages) { stage = 0; phase ^= 1; }
+        if (!ok) break;
+        mma_commit(&sm.qo_empty);
       }
-      if (!ok) break;
-      mma_commit(&sm.qo_empty);
+      if (issued) {
+        mma_commit(&sm.final_bar);
+        drain_wait(&sm.final_bar, 0, p.wait_ns);
+      }
     }
-    if (issued) {
-      mma_commit(&sm.final_bar);
-      drain_wait(&sm.final_bar, 0, p.wait_ns);
-    }
-  } else if (warp >= 4) {
-    const int row = threadIdx.x - 128;  // query row within the tile
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + lane_base, tP = tmem + lane_base + 128;
+  } else {
+    regs_inc<184>();
+    const int g = warp - 4;
+    const int quad = g & 3, half = g >> 2;
+    const int row = quad * 32 + lane;  // query row within the tile
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_base + 64 * half;
+    const uint32_t tP = tmem + lane_base + 128 + 64 * half;
     uint32_t s_phase = 0, d_count = 0;
-    const float sl2 = p.scale_log2, sc = p.scale;
+    const float sl2 = p.scale_log2;
+    const float2 sc2 = make_float2(sl2, sl2);
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
@@ -591,37 +635,41 @@ __global__ void __launch_bounds__(256, 1)
         l2 = (lse == kNegInf) ? kPosInf : lse * kLog2e;
         dl = p.delta[(x.b * p.Hq + x.h) * p.Lq + qrow];
       }
+      const float2 nl = make_float2(-l2, -l2);
+      const float2 nd = make_float2(-dl, -dl);
       bool ok = true;
       for (int64_t j = 0; j < x.nkv; ++j) {
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
         tc_fence_after();
-        // visible key columns: c <= climit
-        const int64_t kb = j * 128;
-        int64_t lim = 127;
-        if (kb + 128 > p.Lk) lim = p.Lk - kb - 1;
+        uint32_t us0[32], us1[32], ud0[32], ud1[32];
+        ld_two_halves(tS, tP, us0, us1, ud0, ud1);
+        // visible key columns of this half: c <= climit
+        const int64_t kb = j * 128 + 64 * half;
+        int64_t lim = 63;
+        if (kb + 64 > p.Lk) lim = p.Lk - kb - 1;
         if (p.causal) {
           const int64_t c2 = p.q_off + qrow - p.kv_off - kb;
           if (c2 < lim) lim = c2;
         }
         const int climit = lim < -1 ? -1 : static_cast<int>(lim);
 #pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t us[32], ud[32];
-          tmem_ld32(tS + cc * 32, us);
-          tmem_ld32(tP + cc * 32, ud);
-          tmem_ld_wait32(us);
-          tmem_ld_wait32(ud);
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t(&us)[32] = cc ? us1 : us0;
+          const uint32_t(&ud)[32] = cc ? ud1 : ud0;
           uint32_t dk[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int c0 = cc * 32 + 2 * e;
-            float p0 = ex2(fmaf(__uint_as_float(us[2 * e]), sl2, -l2));
-            float p1 = ex2(fmaf(__uint_as_float(us[2 * e + 1]), sl2, -l2));
-            if (c0 > climit) p0 = 0.f;
-            if (c0 + 1 > climit) p1 = 0.f;
-            dk[e] = pack_bf16(sc * p0 * (__uint_as_float(ud[2 * e]) - dl),
-                              sc * p1 * (__uint_as_float(ud[2 * e + 1]) - dl));
+            const float2 arg = __ffma2_rn(
+                make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
+            float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+            if (c0 > climit) pr.x = 0.f;
+            if (c0 + 1 > climit) pr.y = 0.f;
+            const float2 dpm = __fadd2_rn(
+                make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
+            const float2 ds = __fmul2_rn(pr, dpm);
+            dk[e] = pack_bf16(ds.x, ds.y);
           }
           tmem_st16(tP + cc * 16, dk);
         }
@@ -635,22 +683,21 @@ __global__ void __launch_bounds__(256, 1)
         if (!mbar_wait(&sm.dq_done, (d_count - 1) & 1, guard)) break;
         tc_fence_after();
       }
+      // epilogue: half h writes dQ columns [D/2 h, D/2 h + D/2) (times scale)
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
+        const int col = (D / 2) * half + cc * 32;
         uint32_t u[32];
         if (x.nkv > 0) {
-          tmem_ld32(tmem + lane_base + 256 + cc * 32, u);
+          tmem_ld32(tmem + lane_base + 256 + col, u);
           tmem_ld_wait32(u);
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
         if (!valid) continue;
-        float vals[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) vals[e] = __uint_as_float(u[e]);
-        store_row32(p.dq, p.dq_f32, x.b * p.dq_sb + x.h * p.dq_sh + qrow * p.dq_sn + cc * 32,
-                    vals, p.accumulate);
+        store_row32(p.dq, p.dq_f32, x.b * p.dq_sb + x.h * p.dq_sh + qrow * p.dq_sn + col, u,
+                    p.scale, p.accumulate);
       }
       tc_fence_before();
     }
@@ -703,7 +750,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDkdv, s);
-    dkdv_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(tq, tk, tv, tdo, p);
+    dkdv_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, tdo, p);
     timing_end(kKidDkdv, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
@@ -716,7 +763,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDq, s);
-    dq_kernel<D><<<static_cast<unsigned>(grid), 256, smem, s>>>(tq, tk, tv, tdo, p);
+    dq_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, tdo, p);
     timing_end(kKidDq, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
