@@ -149,9 +149,11 @@ def run_ours(args, rank, world, local_rank):
     ws_bytes = _lib.load().attn_chunked_bwd_workspace_size(ctypes.byref(vq_), ctypes.byref(vk_),
                                                            w.chunk, 1)
     ws = torch.empty(int(ws_bytes), dtype=torch.uint8, device=dev)
+    ws_f = torch.empty(int(_lib.load().attn_chunked_fwd_workspace_size(
+        ctypes.byref(vq_), ctypes.byref(vk_), w.chunk, 1)), dtype=torch.uint8, device=dev)
 
     def step():
-        lsx.chunked_fwd(q, k, v, w.chunk, causal=True, out=o, lse=lse)
+        lsx.chunked_fwd(q, k, v, w.chunk, causal=True, out=o, lse=lse, workspace=ws_f)
         lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=True, dq=dq, dk=dk, dv=dv,
                         workspace=ws)
 

@@ -91,8 +91,15 @@ typedef struct lsx_tensor {
  *   merged into them in the epilogue (the LSE-weighted merge of attn_merge).
  * D in {64, 128}.  bf16 inputs run on the tcgen05 tensor cores (fp32
  * accumulation, P rounded to bf16 for the P.V product); f32 inputs run an
- * fp32 CUDA-core path.  No workspace is used (workspace may be NULL).
+ * fp32 CUDA-core path.
+ * Workspace (bf16 only, optional): NULL, or at least
+ * attn_chunk_fwd_workspace_size(q, k) bytes, 256-byte aligned.  With it, a
+ * key-contiguous copy of V is written there first and the P.V product reads
+ * that copy, which the tensor cores consume about twice as fast; without
+ * it, V is read as stored.  Both give the same results.  A non-NULL
+ * workspace that is too small returns LSX_ERR_WORKSPACE.
  * ---------------------------------------------------------------------- */
+size_t attn_chunk_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
 int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
                    const lsx_tensor* v, int64_t q_off, int64_t kv_off,
                    int causal, float scale, const lsx_tensor* o,
@@ -143,8 +150,14 @@ int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
  * accumulate == 0: outputs receive this pair's contribution.
  * accumulate == 1: the contribution is added to the outputs (use f32
  *   outputs to sum over many chunk pairs).
- * Workspace: attn_chunk_bwd_workspace_size bytes (row sums D_i = <dO_i,O_i>).
+ * Workspace (256-byte aligned): at least attn_chunk_bwd_min_workspace_size
+ * bytes (the row sums delta_i = <dO_i, O_i>).  With
+ * attn_chunk_bwd_workspace_size bytes (bf16 inputs), sequence-contiguous
+ * copies of Q, dO and K are also written there and the dV, dK, dQ products
+ * read them at the tensor cores' faster operand layout; with less, the
+ * tiles are read as stored.  Both give the same results.
  * ---------------------------------------------------------------------- */
+size_t attn_chunk_bwd_min_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
 size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
 int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
                    const lsx_tensor* v, const lsx_tensor* o,
@@ -163,9 +176,11 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
  * after start-up.  Same tensors, semantics and results as attn_chunk_bwd,
  * but no workspace argument: the row dot products go to a fixed 16 MiB array
  * compiled into the library (attn_chunk_bwd_noalloc_max_bytes()), which every
- * GPU that loads the library holds until the process exits.
- *  - Limit: attn_chunk_bwd_workspace_size(q, k) must not exceed that size
- *    (B * Hq * Lq <= 4,194,304 query rows); larger problems return
+ * GPU that loads the library holds until the process exits; when the
+ * sequence-contiguous operand copies of attn_chunk_bwd also fit, they are
+ * placed there too.
+ *  - Limit: attn_chunk_bwd_min_workspace_size(q, k) must not exceed that
+ *    size (B * Hq * Lq <= 4,194,304 query rows); larger problems return
  *    LSX_ERR_WORKSPACE and launch nothing.
  *  - The array is shared by every call on a device and keeps the last
  *    call's contents (nothing in it needs to start at zero).  Calls whose

@@ -26,11 +26,14 @@ def _ws(nbytes: int, device) -> torch.Tensor:
 
 
 def chunk_fwd(q, k, v, q_off=0, kv_off=0, causal=False, scale=None, out=None,
-              lse=None, accumulate=False, out_dtype=None):
+              lse=None, accumulate=False, out_dtype=None, workspace=None,
+              use_workspace=True):
     """Partial (O, LSE) of one query chunk against one key/value chunk.
 
     With accumulate=True, ``out``/``lse`` must hold a partial over other keys
-    and receive the merged result.
+    and receive the merged result.  use_workspace=False reads V as stored
+    (no scratch); otherwise a workspace for the key-contiguous V copy is
+    allocated here unless one is given.
     """
     lib = load()
     b, h, n, d = q.shape
@@ -39,10 +42,17 @@ def chunk_fwd(q, k, v, q_off=0, kv_off=0, causal=False, scale=None, out=None,
     if lse is None:
         lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
     vq, vk, vv, vo, vl = view(q), view(k), view(v), view(out), view(lse)
+    ws_ptr, ws_n = None, 0
+    if use_workspace:
+        need = lib.attn_chunk_fwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk))
+        if need:
+            if workspace is None:
+                workspace = _ws(need, q.device)
+            ws_ptr, ws_n = workspace.data_ptr(), workspace.numel()
     check(lib.attn_chunk_fwd(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv),
                              int(q_off), int(kv_off), int(bool(causal)), _scale(scale),
                              ctypes.byref(vo), ctypes.byref(vl), int(bool(accumulate)),
-                             None, 0, stream_handle()), "attn_chunk_fwd")
+                             ws_ptr, ws_n, stream_handle()), "attn_chunk_fwd")
     return out, lse
 
 
@@ -79,15 +89,20 @@ def tree_merge(o_parts, lse_parts, out=None, lse_out=None, out_dtype=None):
 
 def chunk_bwd(q, k, v, o, lse, d_o, q_off=0, kv_off=0, causal=False, scale=None,
               dq=None, dk=None, dv=None, accumulate=False, grad_dtype=None,
-              workspace=None):
-    """dQ, dK, dV of one chunk pair from the saved final O and LSE."""
+              workspace=None, use_copies=True):
+    """dQ, dK, dV of one chunk pair from the saved final O and LSE.
+
+    use_copies=False sizes the workspace at the minimum (delta rows only),
+    which makes the kernels read Q, dO, K as stored."""
     lib = load()
     gd = grad_dtype or q.dtype
     dq = torch.empty(q.shape, dtype=gd, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=gd, device=q.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=gd, device=q.device) if dv is None else dv
     vs = [view(t) for t in (q, k, v, o, lse, d_o, dq, dk, dv)]
-    need = lib.attn_chunk_bwd_workspace_size(ctypes.byref(vs[0]), ctypes.byref(vs[1]))
+    size_fn = lib.attn_chunk_bwd_workspace_size if use_copies else \
+        lib.attn_chunk_bwd_min_workspace_size
+    need = size_fn(ctypes.byref(vs[0]), ctypes.byref(vs[1]))
     if workspace is None:
         workspace = _ws(need, q.device)
     check(lib.attn_chunk_bwd(*(ctypes.byref(x) for x in vs[:6]), int(q_off), int(kv_off),
@@ -98,7 +113,8 @@ def chunk_bwd(q, k, v, o, lse, d_o, q_off=0, kv_off=0, causal=False, scale=None,
     return dq, dk, dv
 
 
-def chunked_fwd(q, k, v, chunk_len, causal=True, scale=None, out=None, lse=None):
+def chunked_fwd(q, k, v, chunk_len, causal=True, scale=None, out=None, lse=None,
+                workspace=None):
     """Whole-sequence forward over chunk pairs in one persistent launch."""
     lib = load()
     b, h, n, d = q.shape
@@ -109,7 +125,7 @@ def chunked_fwd(q, k, v, chunk_len, causal=True, scale=None, out=None, lse=None)
     vq, vk, vv, vo, vl = view(q), view(k), view(v), view(out), view(lse)
     need = lib.attn_chunked_fwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk),
                                                int(chunk_len), int(bool(causal)))
-    ws = _ws(need, q.device) if need else None
+    ws = workspace if workspace is not None else (_ws(need, q.device) if need else None)
     check(lib.attn_chunked_fwd(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv),
                                int(chunk_len), int(bool(causal)), _scale(scale),
                                ctypes.byref(vo), ctypes.byref(vl),

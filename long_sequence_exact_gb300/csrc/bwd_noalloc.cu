@@ -13,9 +13,11 @@
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes
 // (16 MiB: delta for up to 4,194,304 query rows, e.g. 32 heads x 131,072
 // tokens).  Every GPU that loads the library keeps it until the process
-// exits.  It is shared by all calls on a device and keeps the last call's
-// contents; nothing in it has to start at zero, because the row-dot kernel
-// writes every delta entry a call uses before the backward kernels read it.
+// exits.  When the sequence-contiguous operand copies that attn_chunk_bwd
+// makes for its faster path also fit, they go into the same array.  It is
+// shared by all calls on a device and keeps the last call's contents;
+// nothing in it has to start at zero, because the row-dot and copy kernels
+// write every entry a call uses before the backward kernels read it.
 // Two calls whose work overlaps on the GPU (e.g. on two streams without an
 // ordering between them) race on the array and produce wrong gradients.
 //
@@ -70,7 +72,7 @@ extern "C" int attn_chunk_bwd_noalloc(const lsx_tensor* q, const lsx_tensor* k,
                                       const lsx_tensor* dk, const lsx_tensor* dv,
                                       int accumulate, lsx_stream_t stream) {
   if (q == nullptr || k == nullptr) return LSX_ERR_NULL;
-  const size_t need = attn_chunk_bwd_workspace_size(q, k);
+  const size_t need = attn_chunk_bwd_min_workspace_size(q, k);
   if (need > lsx::kNoAllocScratchBytes) return LSX_ERR_WORKSPACE;  // beyond the fixed array
   void* scratch = nullptr;
   const int rc = lsx::noalloc_scratch(&scratch);

@@ -76,7 +76,7 @@ struct BwdParams {
 // TMEM column (relative to the 128-column fp32 tile) of the packed bf16
 // operand for K step kk (16 elements = 8 packed columns).
 __device__ __forceinline__ uint32_t packed_col(int kk) {
-  return kk < 4 ? static_cast<uint32_t>(kk * 8) : static_cast<uint32_t>(64 + (kk - 4) * 8);
+  return static_cast<uint32_t>(32 * (kk >> 1) + 8 * (kk & 1));
 }
 
 // First query tile that sees key tile j (n_qtiles when none does).
@@ -142,32 +142,31 @@ __device__ __forceinline__ void store_row32(void* out, int f32, int64_t off,
   }
 }
 
-// Loads 64 fp32 columns (two x32 loads) of two TMEM tiles with one wait.
-__device__ __forceinline__ void ld_two_halves(uint32_t ta, uint32_t tb, uint32_t (&a0)[32],
-                                              uint32_t (&a1)[32], uint32_t (&b0)[32],
-                                              uint32_t (&b1)[32]) {
-  tmem_ld32(ta, a0);
-  tmem_ld32(ta + 32, a1);
-  tmem_ld32(tb, b0);
-  tmem_ld32(tb + 32, b1);
-  tmem_ld_wait32(a0);
-  reg_fence32(a1);
-  reg_fence32(b0);
-  reg_fence32(b1);
+// Loads 32 fp32 columns of two TMEM tiles with one wait.
+__device__ __forceinline__ void ld_two(uint32_t ta, uint32_t tb, uint32_t (&a)[32],
+                                       uint32_t (&b)[32]) {
+  tmem_ld32(ta, a);
+  tmem_ld32(tb, b);
+  tmem_ld_wait32(a);
+  reg_fence32(b);
 }
 
 // ===================================================================== dK dV
+// The dV / dK products read dO and Q as stored (MN-major B operands, the
+// same tiles the S^T / dP^T products use): measured faster here than
+// loading sequence-contiguous copies, whose extra shared-memory traffic
+// slows the SS products more than the K-major reads gain.
 template <int D>
 struct DkdvSmem {
-  static constexpr int kStages = 2;
   __nv_bfloat16 k[128 * D];
   __nv_bfloat16 v[128 * D];
-  __nv_bfloat16 q[kStages][128 * D];
-  __nv_bfloat16 d_o[kStages][128 * D];
-  float lse2[kStages][128];   // LSE * log2(e); +inf for rows without keys
-  float delta[kStages][128];
+  __nv_bfloat16 q[2][128 * D];
+  __nv_bfloat16 d_o[2][128 * D];
+  float lse2[2][128];             // LSE * log2(e); +inf for rows without keys
+  float delta[2][128];
   uint64_t kv_full, kv_empty, final_bar;
-  uint64_t st_full[kStages], st_empty[kStages];
+  uint64_t st_full[2], st_empty[2];
+  uint64_t lse_full[2], lse_empty[2];
   uint64_t s_full, p_full, dkv_done;
   uint32_t tmem_base;
   int abort;
@@ -190,16 +189,58 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
   return x;
 }
 
+// Loads one 128-row tile as D/64 boxes of [128 rows][64 cols] (row-major
+// view, d contiguous) or, from a transposed copy, two boxes of
+// [D rows][64 sequence positions] (sequence contiguous).
+template <int D, bool kTransposed>
+__device__ __forceinline__ void load_tile(__nv_bfloat16* dst, const CUtensorMap* map,
+                                          uint64_t* bar, int64_t row0, int64_t h, int64_t b) {
+  if constexpr (kTransposed) {
+    for (int sub = 0; sub < 2; ++sub)
+      tma_load_4d(dst + sub * D * 64, map, bar, static_cast<int>(row0 + sub * 64), 0,
+                  static_cast<int>(h), static_cast<int>(b));
+  } else {
+    for (int sub = 0; sub < D / 64; ++sub)
+      tma_load_4d(dst + sub * 128 * 64, map, bar, sub * 64, static_cast<int>(row0),
+                  static_cast<int>(h), static_cast<int>(b));
+  }
+}
+
+// S-type product D (+)= A B^T over K = D, both operands K-major 128-row
+// tiles; base descriptors are built once and stepped by constants so that
+// the single issuing thread keeps ahead of the tensor pipe.
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__device__ __forceinline__ void mma_rows_by_rows(uint32_t d_tmem, uint32_t a_addr,
+                                                 uint32_t b_addr, uint32_t idesc) {
+  const uint64_t a0 = sdesc_sw128(a_addr, 16, 1024);
+  const uint64_t b0 = sdesc_sw128(b_addr, 16, 1024);
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk)
+    mma_ss(d_tmem, a0 + kmajor_step(kk, 128), b0 + kmajor_step(kk, 128), idesc,
+           kk > 0 ? 1u : 0u);
+}
+
+// Base descriptor and per-step offset of a B operand spanning a 128-row
+// tile of the sequence: K-major from a transposed tile (D rows of 128
+// positions), MN-major from the row-major tile.
+template <int D, bool kTransposed>
+__device__ __forceinline__ uint64_t seq_b_base(uint32_t base) {
+  return kTransposed ? sdesc_sw128(base, 16, 1024) : sdesc_sw128(base, 128 * 128, 1024);
+}
+template <int D, bool kTransposed>
+__host__ __device__ constexpr uint64_t seq_b_step(int kk) {
+  return kTransposed ? kmajor_step(kk, D) : mnmajor_step(kk);
+}
+
+template <int D>
+__global__ void __launch_bounds__(640, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
   using Sm = DkdvSmem<D>;
-  constexpr int kStages = Sm::kStages;
   constexpr int kTile = 128 * D * 2;
-  constexpr int kSub = D / 64;
+  constexpr int kQoStages = 2;
   extern __shared__ uint8_t smem_raw[];
   Sm& sm = *reinterpret_cast<Sm*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                   ~uintptr_t(1023));
@@ -210,12 +251,14 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     mbar_init(&sm.final_bar, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.st_full[s], 32);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sm.st_full[s], 1);
       mbar_init(&sm.st_empty[s], 1);
+      mbar_init(&sm.lse_full[s], 32);
+      mbar_init(&sm.lse_empty[s], 512);
     }
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 256);
+    mbar_init(&sm.p_full, 512);
     mbar_init(&sm.dkv_done, 1);
     fence_barrier_init();
   }
@@ -229,14 +272,14 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
 
-  // 384 threads launched at <= 168 registers (64,512): the load/MMA
-  // warpgroup keeps 88, the two grad warpgroups take 184:
-  // 128 * 88 + 256 * 184 = 58,368 <= 64,512.
+  // 640 threads launched at <= 96 registers (61,440): the load/MMA
+  // warpgroup keeps 64, the four grad warpgroups take 104:
+  // 128 * 64 + 512 * 104 = 61,440 <= 61,440.
   if (warp < 4) {
-    regs_dec<88>();
+    regs_dec<64>();
     if (warp == 0) {
       // -------------------------------------------------- loads (warp 0)
-      uint32_t stage = 0, phase = 0, kv_phase = 0;
+      uint32_t qs = 0, qph = 0, ls = 0, lph = 0, kv_phase = 0;
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
@@ -245,21 +288,23 @@ __global__ void __launch_bounds__(384, 1)
         kv_phase ^= 1;
         if (lane == 0) {
           mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-          for (int sub = 0; sub < kSub; ++sub) {
-            tma_load_4d(&sm.k[sub * 128 * 64], &tm_k, &sm.kv_full, sub * 64,
-                        static_cast<int>(x.j * 128), static_cast<int>(x.hk),
-                        static_cast<int>(x.b));
-            tma_load_4d(&sm.v[sub * 128 * 64], &tm_v, &sm.kv_full, sub * 64,
-                        static_cast<int>(x.j * 128), static_cast<int>(x.hk),
-                        static_cast<int>(x.b));
-          }
+          load_tile<D, false>(sm.k, &tm_k, &sm.kv_full, x.j * 128, x.hk, x.b);
+          load_tile<D, false>(sm.v, &tm_v, &sm.kv_full, x.j * 128, x.hk, x.b);
         }
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
           const int64_t h = x.hk * x.group + s / (p.n_qtiles - x.i0);
           const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
-          if (!mbar_wait(&sm.st_empty[stage], phase ^ 1, guard)) { ok = false; break; }
-          // LSE (as log2 units) and delta of the 128 query rows of tile i
+          // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV)
+          if (!mbar_wait(&sm.st_empty[qs], qph ^ 1, guard)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.st_full[qs], 2 * kTile);
+            load_tile<D, false>(sm.q[qs], &tm_q, &sm.st_full[qs], i * 128, h, x.b);
+            load_tile<D, false>(sm.d_o[qs], &tm_do, &sm.st_full[qs], i * 128, h, x.b);
+          }
+          if (++qs == kQoStages) { qs = 0; qph ^= 1; }
+          // LSE (log2 units) and delta of the 128 query rows of tile i
+          if (!mbar_wait(&sm.lse_empty[ls], lph ^ 1, guard)) { ok = false; break; }
           for (int t = lane; t < 128; t += 32) {
             const int64_t row = i * 128 + t;
             float l2 = kPosInf, dl = 0.f;
@@ -268,22 +313,11 @@ __global__ void __launch_bounds__(384, 1)
               l2 = (lse == kNegInf) ? kPosInf : lse * kLog2e;
               dl = p.delta[(x.b * p.Hq + h) * p.Lq + row];
             }
-            sm.lse2[stage][t] = l2;
-            sm.delta[stage][t] = dl;
+            sm.lse2[ls][t] = l2;
+            sm.delta[ls][t] = dl;
           }
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.st_full[stage], 2 * kTile);
-            for (int sub = 0; sub < kSub; ++sub) {
-              tma_load_4d(&sm.q[stage][sub * 128 * 64], &tm_q, &sm.st_full[stage], sub * 64,
-                          static_cast<int>(i * 128), static_cast<int>(h), static_cast<int>(x.b));
-              tma_load_4d(&sm.d_o[stage][sub * 128 * 64], &tm_do, &sm.st_full[stage],
-                          sub * 64, static_cast<int>(i * 128), static_cast<int>(h),
-                          static_cast<int>(x.b));
-            }
-          } else {
-            mbar_arrive(&sm.st_full[stage]);
-          }
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          mbar_arrive(&sm.lse_full[ls]);
+          if (++ls == 2) { ls = 0; lph ^= 1; }
         }
         if (!ok) break;
       }
@@ -291,7 +325,7 @@ __global__ void __launch_bounds__(384, 1)
       // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
-      uint32_t stage = 0, phase = 0, kv_phase = 0, p_phase = 0;
+      uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0;
       bool issued = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
       for (int64_t r = 0;; ++r) {
@@ -303,38 +337,32 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
-          if (!mbar_wait(&sm.st_full[stage], phase, guard)) { ok = false; break; }
+          if (!mbar_wait(&sm.st_full[qs], qph, guard)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t q_addr = smem_addr(sm.q[stage]);
-          const uint32_t o_addr = smem_addr(sm.d_o[stage]);
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tmem + 0, sdesc_sw128(k_addr + off, 16, 1024),
-                   sdesc_sw128(q_addr + off, 16, 1024), kIdS, kk > 0);
-          }
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tmem + 128, sdesc_sw128(v_addr + off, 16, 1024),
-                   sdesc_sw128(o_addr + off, 16, 1024), kIdS, kk > 0);
-          }
+          const uint32_t q_addr = smem_addr(sm.q[qs]);
+          const uint32_t o_addr = smem_addr(sm.d_o[qs]);
+          mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
+          mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
           mma_commit(&sm.s_full);
           issued = true;
           if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
           p_phase ^= 1;
+          const uint32_t bq = q_addr, bo = o_addr;
           tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint32_t acc = (s > 0 || kk > 0) ? 1u : 0u;
-            mma_ts(tmem + 256, tmem + packed_col(kk),
-                   sdesc_sw128(o_addr + kk * 2048, 128 * 128, 1024), kIdG, acc);
-            mma_ts(tmem + 384, tmem + 128 + packed_col(kk),
-                   sdesc_sw128(q_addr + kk * 2048, 128 * 128, 1024), kIdG, acc);
+          {
+            const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
+            const uint32_t acc0 = s > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t acc = kk > 0 ? 1u : acc0;
+              mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG, acc);
+              mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
+                     acc);
+            }
           }
           mma_commit(&sm.dkv_done);
-          mma_commit(&sm.st_empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          mma_commit(&sm.st_empty[qs]);
+          if (++qs == kQoStages) { qs = 0; qph ^= 1; }
         }
         if (!ok) break;
         mma_commit(&sm.kv_empty);
@@ -345,15 +373,15 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else {
-    regs_inc<184>();
+    regs_inc<104>();
     // -------------------------------------------- P^T, dS^T and the epilogue
     const int g = warp - 4;
-    const int quad = g & 3, half = g >> 2;
+    const int quad = g & 3, qtr = g >> 2;
     const int row = quad * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + 64 * half;        // S^T / P^T
-    const uint32_t tP = tmem + lane_base + 128 + 64 * half;  // dP^T / dS^T
-    uint32_t stage = 0, phase = 0, s_phase = 0;
+    const uint32_t tS = tmem + lane_base + 32 * qtr;        // S^T / P^T
+    const uint32_t tP = tmem + lane_base + 128 + 32 * qtr;  // dP^T / dS^T
+    uint32_t ls = 0, lph = 0, s_phase = 0;
     uint32_t d_count = 0;
     const float sl2 = p.scale_log2;
     const float2 sc2 = make_float2(sl2, sl2);
@@ -367,24 +395,21 @@ __global__ void __launch_bounds__(384, 1)
         const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
-        // the stage's LSE/delta rows were published with st_full
-        if (!mbar_wait(&sm.st_full[stage], phase, guard)) { ok = false; break; }
+        if (!mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
         tc_fence_after();
-        uint32_t us0[32], us1[32], ud0[32], ud1[32];
-        ld_two_halves(tS, tP, us0, us1, ud0, ud1);
-        // query columns c (of this half) with q_off + 128 i + 64 half + c >=
-        // key_abs are visible
+        uint32_t us[32], ud[32];
+        ld_two(tS, tP, us, ud);
+        // query columns c (of this quarter) with q_off + 128 i + 32 qtr + c
+        // >= key_abs are visible
         int cmin = 0;
         if (p.causal) {
-          const int64_t tt = key_abs - (p.q_off + i * 128 + 64 * half);
-          cmin = tt <= 0 ? 0 : (tt > 64 ? 64 : static_cast<int>(tt));
+          const int64_t tt = key_abs - (p.q_off + i * 128 + 32 * qtr);
+          cmin = tt <= 0 ? 0 : (tt > 32 ? 32 : static_cast<int>(tt));
         }
-        const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[stage][64 * half]);
-        const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[stage][64 * half]);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const uint32_t(&us)[32] = cc ? us1 : us0;
-          const uint32_t(&ud)[32] = cc ? ud1 : ud0;
+        const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[ls][32 * qtr]);
+        const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[ls][32 * qtr]);
+        {
+          constexpr int cc = 0;
           uint32_t pk[16], dk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
@@ -411,11 +436,12 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st16(tS + cc * 16, pk);
           tmem_st16(tP + cc * 16, dk);
         }
+        mbar_arrive(&sm.lse_empty[ls]);
+        if (++ls == 2) { ls = 0; lph ^= 1; }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full);
         ++d_count;
-        if (++stage == DkdvSmem<D>::kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
       // epilogue: half 0 writes dV, half 1 writes dK (times scale)
@@ -425,9 +451,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       const int64_t krow = x.j * 128 + row;
       const bool valid = krow < p.Lk;
-      const uint32_t base_col = half == 0 ? 256u : 384u;
+      // quarters 0, 1: dV columns [0, D/2), [D/2, D); quarters 2, 3: dK
+      const uint32_t base_col = (qtr < 2 ? 256u : 384u) + (qtr & 1) * (D / 2);
+      const int col0 = (qtr & 1) * (D / 2);
 #pragma unroll
-      for (int cc = 0; cc < D / 32; ++cc) {
+      for (int cc = 0; cc < D / 64; ++cc) {
         uint32_t u[32];
         if (x.n_i > 0) {
           tmem_ld32(tmem + lane_base + base_col + cc * 32, u);
@@ -437,12 +465,14 @@ __global__ void __launch_bounds__(384, 1)
           for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
         if (!valid) continue;
-        if (half == 0)
-          store_row32(p.dv, p.dv_f32, x.b * p.dv_sb + x.hk * p.dv_sh + krow * p.dv_sn + cc * 32,
-                      u, 1.f, p.accumulate);
+        if (qtr < 2)
+          store_row32(p.dv, p.dv_f32,
+                      x.b * p.dv_sb + x.hk * p.dv_sh + krow * p.dv_sn + col0 + cc * 32, u, 1.f,
+                      p.accumulate);
         else
-          store_row32(p.dk, p.dk_f32, x.b * p.dk_sb + x.hk * p.dk_sh + krow * p.dk_sn + cc * 32,
-                      u, p.scale, p.accumulate);
+          store_row32(p.dk, p.dk_f32,
+                      x.b * p.dk_sb + x.hk * p.dk_sh + krow * p.dk_sn + col0 + cc * 32, u,
+                      p.scale, p.accumulate);
       }
       tc_fence_before();
     }
@@ -457,16 +487,23 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ======================================================================= dQ
-template <int D>
+// Query-tile-major.  S = Q K_j^T and dP = dO V_j^T (SS), dS -> bf16 pairs in
+// its own TMEM columns, dQ += dS K_j (TS).  The grad warps release the S/dP
+// columns as soon as they have loaded them, so the next S/dP products run
+// while they compute dS, and dQ(j) runs while dS(j+1) is being computed.
+// TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS [384,448).
+template <int D, bool kT>
 struct DqSmem {
   static constexpr int kStages = 2;
   __nv_bfloat16 q[128 * D];
   __nv_bfloat16 d_o[128 * D];
   __nv_bfloat16 k[kStages][128 * D];
   __nv_bfloat16 v[kStages][128 * D];
+  __nv_bfloat16 kt[kT ? 128 * D : 8];
   uint64_t qo_full, qo_empty, final_bar;
   uint64_t kv_full[kStages], kv_empty[kStages];
-  uint64_t s_full, p_full, dq_done;
+  uint64_t kt_full, kt_empty;
+  uint64_t s_full, s_free, p_full, ds_free;
   uint32_t tmem_base;
   int abort;
 };
@@ -487,16 +524,16 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int64_t it) {
   return x;
 }
 
-template <int D>
-__global__ void __launch_bounds__(384, 1)
+template <int D, bool kT>
+__global__ void __launch_bounds__(640, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v,
-              const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
-  using Sm = DqSmem<D>;
+              const __grid_constant__ CUtensorMap tm_do,
+              const __grid_constant__ CUtensorMap tm_kt, const BwdParams p) {
+  using Sm = DqSmem<D, kT>;
   constexpr int kStages = Sm::kStages;
   constexpr int kTile = 128 * D * 2;
-  constexpr int kSub = D / 64;
   extern __shared__ uint8_t smem_raw[];
   Sm& sm = *reinterpret_cast<Sm*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                   ~uintptr_t(1023));
@@ -511,9 +548,12 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&sm.kv_full[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
+    mbar_init(&sm.kt_full, 1);
+    mbar_init(&sm.kt_empty, 1);
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 256);
-    mbar_init(&sm.dq_done, 1);
+    mbar_init(&sm.s_free, 512);
+    mbar_init(&sm.p_full, 512);
+    mbar_init(&sm.ds_free, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -526,83 +566,108 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
 
-  // same register split as dkdv_kernel: 128 * 88 + 256 * 184 <= 384 * 168
+  // 640 threads launched at <= 96 registers (61,440): the load/MMA
+  // warpgroup keeps 64, the four grad warpgroups take 104:
+  // 128 * 64 + 512 * 104 = 61,440 <= 61,440.
   if (warp < 4) {
-    regs_dec<88>();
+    regs_dec<64>();
     if (warp == 0 && lane == 0) {
+      // ------------------------------------------- loads: Q, dO and K/V ring
       uint32_t stage = 0, phase = 0, qo_phase = 0;
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
         const DqItem x = dq_item(p, it);
+        if (x.nkv == 0) continue;
         if (!mbar_wait(&sm.qo_empty, qo_phase ^ 1, guard)) break;
         qo_phase ^= 1;
         mbar_arrive_expect_tx(&sm.qo_full, 2 * kTile);
-        for (int sub = 0; sub < kSub; ++sub) {
-          tma_load_4d(&sm.q[sub * 128 * 64], &tm_q, &sm.qo_full, sub * 64,
-                      static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
-          tma_load_4d(&sm.d_o[sub * 128 * 64], &tm_do, &sm.qo_full, sub * 64,
-                      static_cast<int>(x.i * 128), static_cast<int>(x.h), static_cast<int>(x.b));
-        }
+        load_tile<D, false>(sm.q, &tm_q, &sm.qo_full, x.i * 128, x.h, x.b);
+        load_tile<D, false>(sm.d_o, &tm_do, &sm.qo_full, x.i * 128, x.h, x.b);
         bool ok = true;
         for (int64_t j = 0; j < x.nkv; ++j) {
           if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.kv_full[stage], 2 * kTile);
-          for (int sub = 0; sub < kSub; ++sub) {
-            tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.kv_full[stage], sub * 64,
-                        static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
-            tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.kv_full[stage], sub * 64,
-                        static_cast<int>(j * 128), static_cast<int>(x.hk), static_cast<int>(x.b));
-          }
+          load_tile<D, false>(sm.k[stage], &tm_k, &sm.kv_full[stage], j * 128, x.hk, x.b);
+          load_tile<D, false>(sm.v[stage], &tm_v, &sm.kv_full[stage], j * 128, x.hk, x.b);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
       }
+    } else if (kT && warp == 0 && lane == 1) {
+      // ------------------------- loads: K^T ring (its own thread, so that a
+      // K^T slot still in use never holds back the K/V prefetch)
+      uint32_t kt_phase = 0;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DqItem x = dq_item(p, it);
+        bool ok = true;
+        for (int64_t j = 0; j < x.nkv; ++j) {
+          if (!mbar_wait(&sm.kt_empty, kt_phase ^ 1, guard)) { ok = false; break; }
+          kt_phase ^= 1;
+          mbar_arrive_expect_tx(&sm.kt_full, kTile);
+          load_tile<D, true>(sm.kt, &tm_kt, &sm.kt_full, j * 128, x.hk, x.b);
+        }
+        if (!ok) break;
+      }
     } else if (warp == 1 && lane == 0) {
+      // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
-      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
-      uint32_t stage = 0, phase = 0, qo_phase = 0, p_phase = 0;
-      bool issued = false;
+      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, kT ? 0 : 1);
+      uint32_t kst = 0, kph = 0, kt_phase = 0, qo_phase = 0, sf_phase = 0, pf_phase = 0;
+      bool s_outstanding = false, issued = false;
       const uint32_t q_addr = smem_addr(sm.q), o_addr = smem_addr(sm.d_o);
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
         const DqItem x = dq_item(p, it);
+        if (x.nkv == 0) continue;
         if (!mbar_wait(&sm.qo_full, qo_phase, guard)) break;
         qo_phase ^= 1;
         tc_fence_after();
         bool ok = true;
-        for (int64_t j = 0; j < x.nkv; ++j) {
-          if (!mbar_wait(&sm.kv_full[stage], phase, guard)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t k_addr = smem_addr(sm.k[stage]);
-          const uint32_t v_addr = smem_addr(sm.v[stage]);
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tmem + 0, sdesc_sw128(q_addr + off, 16, 1024),
-                   sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
+        uint32_t prev = 0;
+        for (int64_t j = 0; j <= x.nkv; ++j) {
+          const uint32_t cur = kst;
+          if (j < x.nkv) {
+            if (!mbar_wait(&sm.kv_full[kst], kph, guard)) { ok = false; break; }
+            if (s_outstanding) {  // the grad warps have loaded the last S/dP
+              if (!mbar_wait(&sm.s_free, sf_phase, guard)) { ok = false; break; }
+              sf_phase ^= 1;
+            }
+            tc_fence_after();
+            mma_rows_by_rows<D>(tmem + 0, q_addr, smem_addr(sm.k[kst]), kIdS);
+            mma_rows_by_rows<D>(tmem + 128, o_addr, smem_addr(sm.v[kst]), kIdS);
+            mma_commit(&sm.s_full);
+            s_outstanding = true;
+            issued = true;
+            if constexpr (kT) mma_commit(&sm.kv_empty[kst]);  // K_j, V_j done
+            if (++kst == kStages) { kst = 0; kph ^= 1; }
           }
-#pragma unroll 1
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(tmem + 128, sdesc_sw128(o_addr + off, 16, 1024),
-                   sdesc_sw128(v_addr + off, 16, 1024), kIdS, kk > 0);
+          if (j > 0) {  // dQ += dS(j-1) K_{j-1}
+            if (!mbar_wait(&sm.p_full, pf_phase, guard)) { ok = false; break; }
+            pf_phase ^= 1;
+            uint64_t b0;
+            if constexpr (kT) {
+              if (!mbar_wait(&sm.kt_full, kt_phase, guard)) { ok = false; break; }
+              kt_phase ^= 1;
+              b0 = sdesc_sw128(smem_addr(sm.kt), 16, 1024);
+            } else {
+              b0 = sdesc_sw128(smem_addr(sm.k[prev]), 128 * 128, 1024);
+            }
+            tc_fence_after();
+            const uint32_t acc0 = j > 1 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + 256, tmem + 384 + kk * 8,
+                     b0 + (kT ? kmajor_step(kk, D) : mnmajor_step(kk)), kIdG,
+                     kk > 0 ? 1u : acc0);
+            mma_commit(&sm.ds_free);
+            if constexpr (kT) mma_commit(&sm.kt_empty);
+            else mma_commit(&sm.kv_empty[prev]);
           }
-          mma_commit(&sm.s_full);
-          issued = true;
-          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
-          p_phase ^= 1;
-          tc_fence_after();
-#pragma unroll 1
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ts(tmem + 256, tmem + 128 + packed_col(kk),
-                   sdesc_sw128(k_addr + kk * 2048, 128 * 128, 1024), kIdG,
-                   (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&sm.dq_done);
-          mma_commit(&sm.kv_empty[stage]);
-          if (++stage == kStages) { stage = 0; phase ^= 1; }
+          prev = cur;
         }
         if (!ok) break;
         mma_commit(&sm.qo_empty);
@@ -613,14 +678,16 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else {
-    regs_inc<184>();
+    regs_inc<104>();
+    // ------------------------------------------------------ dS and epilogue
     const int g = warp - 4;
-    const int quad = g & 3, half = g >> 2;
-    const int row = quad * 32 + lane;  // query row within the tile
+    const int quad = g & 3, qtr = g >> 2;
+    const int row = quad * 32 + lane;  // query row within the tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t tS = tmem + lane_base + 64 * half;
-    const uint32_t tP = tmem + lane_base + 128 + 64 * half;
-    uint32_t s_phase = 0, d_count = 0;
+    const uint32_t tS = tmem + lane_base + 32 * qtr;
+    const uint32_t tP = tmem + lane_base + 128 + 32 * qtr;
+    const uint32_t tD = tmem + lane_base + 384 + 16 * qtr;  // packed dS of this quarter
+    uint32_t s_phase = 0, n_ds = 0;
     const float sl2 = p.scale_log2;
     const float2 sc2 = make_float2(sl2, sl2);
     for (int64_t r = 0;; ++r) {
@@ -629,6 +696,14 @@ __global__ void __launch_bounds__(384, 1)
       const DqItem x = dq_item(p, it);
       const int64_t qrow = x.i * 128 + row;
       const bool valid = qrow < p.Lq;
+      if (x.nkv == 0) {  // no visible key: dQ = 0 (or unchanged when accumulating)
+        if (valid && !p.accumulate && 32 * qtr < D) {
+          uint32_t z[32] = {};
+          store_row32(p.dq, p.dq_f32, x.b * p.dq_sb + x.h * p.dq_sh + qrow * p.dq_sn + 32 * qtr,
+                      z, 0.f, 0);
+        }
+        continue;
+      }
       float l2 = kPosInf, dl = 0.f;
       if (valid) {
         const float lse = p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn];
@@ -642,62 +717,56 @@ __global__ void __launch_bounds__(384, 1)
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
         tc_fence_after();
-        uint32_t us0[32], us1[32], ud0[32], ud1[32];
-        ld_two_halves(tS, tP, us0, us1, ud0, ud1);
-        // visible key columns of this half: c <= climit
-        const int64_t kb = j * 128 + 64 * half;
-        int64_t lim = 63;
-        if (kb + 64 > p.Lk) lim = p.Lk - kb - 1;
+        uint32_t us[32], ud[32];
+        ld_two(tS, tP, us, ud);
+        tc_fence_before();
+        mbar_arrive(&sm.s_free);  // S/dP columns may be overwritten now
+        // visible key columns of this quarter: c <= climit
+        const int64_t kb = j * 128 + 32 * qtr;
+        int64_t lim = 31;
+        if (kb + 32 > p.Lk) lim = p.Lk - kb - 1;
         if (p.causal) {
           const int64_t c2 = p.q_off + qrow - p.kv_off - kb;
           if (c2 < lim) lim = c2;
         }
         const int climit = lim < -1 ? -1 : static_cast<int>(lim);
+        uint32_t dk[16];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const uint32_t(&us)[32] = cc ? us1 : us0;
-          const uint32_t(&ud)[32] = cc ? ud1 : ud0;
-          uint32_t dk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = cc * 32 + 2 * e;
-            const float2 arg = __ffma2_rn(
-                make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
-            float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
-            if (c0 > climit) pr.x = 0.f;
-            if (c0 + 1 > climit) pr.y = 0.f;
-            const float2 dpm = __fadd2_rn(
-                make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
-            const float2 ds = __fmul2_rn(pr, dpm);
-            dk[e] = pack_bf16(ds.x, ds.y);
-          }
-          tmem_st16(tP + cc * 16, dk);
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = 2 * e;
+          const float2 arg = __ffma2_rn(
+              make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
+          float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+          if (c0 > climit) pr.x = 0.f;
+          if (c0 + 1 > climit) pr.y = 0.f;
+          const float2 dpm = __fadd2_rn(
+              make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
+          const float2 ds = __fmul2_rn(pr, dpm);
+          dk[e] = pack_bf16(ds.x, ds.y);
         }
+        // the dS columns are free once the previous dQ product has read them
+        if (n_ds > 0) {
+          if (!mbar_wait(&sm.ds_free, (n_ds - 1) & 1, guard)) { ok = false; break; }
+          tc_fence_after();
+        }
+        tmem_st16(tD, dk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full);
-        ++d_count;
+        ++n_ds;
       }
       if (!ok) break;
-      if (x.nkv > 0) {
-        if (!mbar_wait(&sm.dq_done, (d_count - 1) & 1, guard)) break;
-        tc_fence_after();
-      }
-      // epilogue: half h writes dQ columns [D/2 h, D/2 h + D/2) (times scale)
-#pragma unroll
-      for (int cc = 0; cc < D / 64; ++cc) {
-        const int col = (D / 2) * half + cc * 32;
+      if (!mbar_wait(&sm.ds_free, (n_ds - 1) & 1, guard)) break;
+      tc_fence_after();
+      // epilogue: quarter q writes dQ columns [32 q, 32 q + 32) (times scale)
+      if (32 * qtr < D) {
         uint32_t u[32];
-        if (x.nkv > 0) {
-          tmem_ld32(tmem + lane_base + 256 + col, u);
-          tmem_ld_wait32(u);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = 0u;
-        }
-        if (!valid) continue;
-        store_row32(p.dq, p.dq_f32, x.b * p.dq_sb + x.h * p.dq_sh + qrow * p.dq_sn + col, u,
-                    p.scale, p.accumulate);
+        tmem_ld32(tmem + lane_base + 256 + 32 * qtr, u);
+        tmem_ld_wait32(u);
+        if (valid)
+          store_row32(p.dq, p.dq_f32,
+                      x.b * p.dq_sb + x.h * p.dq_sh + qrow * p.dq_sn + 32 * qtr, u, p.scale,
+                      p.accumulate);
       }
       tc_fence_before();
     }
@@ -711,19 +780,35 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+bool map_rows(CUtensorMap* m, const lsx_tensor& t) {
+  return make_map_bf16_4d(m, t.data, t.B, t.H, t.N, t.D, t.stride_b, t.stride_h, t.stride_n,
+                          128);
+}
+
+// map over a transposed copy [B, H, D, Np] of t (boxes of 64 positions x D rows)
+bool map_transposed(CUtensorMap* m, const lsx_tensor& t, void* copy, int box_rows) {
+  const int64_t np = transposed_row_len(t.N);
+  return make_map_bf16_4d(m, copy, t.B, t.H, t.D, t.N, t.H * t.D * np, t.D * np, np, box_rows);
+}
+
 template <int D>
 int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                     const lsx_tensor& lse, const lsx_tensor& d_o, const float* delta,
-                    int64_t q_off, int64_t kv_off, int causal, float scale,
-                    const lsx_tensor& dq, const lsx_tensor& dk, const lsx_tensor& dv,
-                    int accumulate, const DeviceCtx& ctx, cudaStream_t s) {
-  CUtensorMap tq, tk, tv, tdo;
-  if (!make_map_bf16_4d(&tq, q.data, q.B, q.H, q.N, q.D, q.stride_b, q.stride_h, q.stride_n, 128) ||
-      !make_map_bf16_4d(&tk, k.data, k.B, k.H, k.N, k.D, k.stride_b, k.stride_h, k.stride_n, 128) ||
-      !make_map_bf16_4d(&tv, v.data, v.B, v.H, v.N, v.D, v.stride_b, v.stride_h, v.stride_n, 128) ||
-      !make_map_bf16_4d(&tdo, d_o.data, d_o.B, d_o.H, d_o.N, d_o.D, d_o.stride_b, d_o.stride_h,
-                        d_o.stride_n, 128))
+                    const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
+                    float scale, const lsx_tensor& dq, const lsx_tensor& dk,
+                    const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
+                    cudaStream_t s) {
+  const bool tr = cp.kt != nullptr;
+  CUtensorMap tq, tk, tv, tdo, tkt;
+  if (!map_rows(&tq, q) || !map_rows(&tk, k) || !map_rows(&tv, v) || !map_rows(&tdo, d_o))
     return LSX_ERR_LAUNCH;
+  if (tr) {
+    const int rc = launch_transpose(k, cp.kt, s);
+    if (rc != LSX_OK) return rc;
+    if (!map_transposed(&tkt, k, cp.kt, D)) return LSX_ERR_LAUNCH;
+  } else {
+    tkt = tk;
+  }
   BwdParams p;
   p.B = q.B; p.Hq = q.H; p.Hkv = k.H; p.Lq = q.N; p.Lk = k.N;
   p.q_off = q_off; p.kv_off = kv_off; p.causal = causal; p.accumulate = accumulate;
@@ -745,25 +830,27 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.n_items = p.n_ktiles * q.B * k.H;
   {
     const size_t smem = sizeof(DkdvSmem<D>) + 1024;
-    if (cudaFuncSetAttribute(dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = dkdv_kernel<D>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDkdv, s);
-    dkdv_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, tdo, p);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, p);
     timing_end(kKidDkdv, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
   // dQ: items (query tile, b, head)
   p.n_items = p.n_qtiles * q.B * q.H;
   {
-    const size_t smem = sizeof(DqSmem<D>) + 1024;
-    if (cudaFuncSetAttribute(dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = (tr ? sizeof(DqSmem<D, true>) : sizeof(DqSmem<D, false>)) + 1024;
+    auto kern = tr ? dq_kernel<D, true> : dq_kernel<D, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDq, s);
-    dq_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, tdo, p);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, tkt, p);
     timing_end(kKidDq, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
@@ -772,17 +859,31 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
 
 }  // namespace
 
+size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k) {
+  (void)q;
+  return (transposed_bytes(k) + 255) / 256 * 256;
+}
+
+BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base) {
+  (void)q;
+  (void)k;
+  BwdCopies c;
+  c.kt = base;
+  return c;
+}
+
 int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                   const lsx_tensor& lse, const lsx_tensor& d_o, const float* delta,
-                  int64_t q_off, int64_t kv_off, int causal, float scale,
-                  const lsx_tensor& dq, const lsx_tensor& dk, const lsx_tensor& dv,
-                  int accumulate, const DeviceCtx& ctx, cudaStream_t s) {
+                  const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
+                  float scale, const lsx_tensor& dq, const lsx_tensor& dk,
+                  const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
+                  cudaStream_t s) {
   if (q.D == 128)
-    return launch_bwd_tc_d<128>(q, k, v, lse, d_o, delta, q_off, kv_off, causal, scale, dq, dk,
-                                dv, accumulate, ctx, s);
+    return launch_bwd_tc_d<128>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
+                                dk, dv, accumulate, ctx, s);
   if (q.D == 64)
-    return launch_bwd_tc_d<64>(q, k, v, lse, d_o, delta, q_off, kv_off, causal, scale, dq, dk,
-                               dv, accumulate, ctx, s);
+    return launch_bwd_tc_d<64>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
+                               dk, dv, accumulate, ctx, s);
   return LSX_ERR_UNSUPPORTED;
 }
 

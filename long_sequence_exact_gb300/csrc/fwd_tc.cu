@@ -118,7 +118,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
-template <int D>
+template <int D, bool kVt>
 __global__ void __launch_bounds__(384, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -195,10 +195,18 @@ __global__ void __launch_bounds__(384, 1)
                       static_cast<int>(x.hk), static_cast<int>(x.b));
         if (!mbar_wait(&sm.v_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.v_full[stage], Cfg::kTileBytes);
-        for (int sub = 0; sub < Cfg::kSub; ++sub)
-          tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.v_full[stage],
-                      sub * 64, static_cast<int>(j * 128),
-                      static_cast<int>(x.hk), static_cast<int>(x.b));
+        if constexpr (kVt) {
+          // V^T tile: D rows (d) x 128 keys, as two 64-key boxes
+          for (int sub = 0; sub < 2; ++sub)
+            tma_load_4d(&sm.v[stage][sub * D * 64], &tm_v, &sm.v_full[stage],
+                        static_cast<int>(j * 128 + sub * 64), 0,
+                        static_cast<int>(x.hk), static_cast<int>(x.b));
+        } else {
+          for (int sub = 0; sub < Cfg::kSub; ++sub)
+            tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.v_full[stage],
+                        sub * 64, static_cast<int>(j * 128),
+                        static_cast<int>(x.hk), static_cast<int>(x.b));
+        }
         if (++stage == kStages) { stage = 0; phase ^= 1; }
       }
       if (!ok) break;
@@ -206,7 +214,7 @@ __global__ void __launch_bounds__(384, 1)
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
-    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, 0, 1);
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, 0, kVt ? 0 : 1);
     // Order per key tile j:  P_0 V_j, S_0 = Q_0 K_{j+1}^T, P_1 V_j, S_1 = ...
     // S_t(j+1) overwrites the TMEM columns that P_t(j) occupies; it is
     // issued right after P_t(j) V_j by this same thread, and one thread's
@@ -218,13 +226,14 @@ __global__ void __launch_bounds__(384, 1)
     uint32_t p_phase[2] = {0, 0};
     bool issued = false;
     const uint32_t q_addr[2] = {smem_addr(sm.q[0]), smem_addr(sm.q[1])};
+    const uint64_t q_desc[2] = {sdesc_sw128(q_addr[0], 16, 1024),
+                                sdesc_sw128(q_addr[1], 16, 1024)};
     auto issue_s = [&](int t, uint32_t k_addr) {
+      const uint64_t k0 = sdesc_sw128(k_addr, 16, 1024);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-        mma_ss(tmem + t * 128, sdesc_sw128(q_addr[t] + off, 16, 1024),
-               sdesc_sw128(k_addr + off, 16, 1024), kIdS, kk > 0);
-      }
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + t * 128, q_desc[t] + kmajor_step(kk, 128), k0 + kmajor_step(kk, 128),
+               kIdS, kk > 0 ? 1u : 0u);
       mma_commit(&sm.s_full[t]);
     };
     for (int64_t r = 0;; ++r) {
@@ -256,11 +265,17 @@ __global__ void __launch_bounds__(384, 1)
             if (!mbar_wait(&sm.p_full[t], p_phase[t], guard)) { ok = false; break; }
             p_phase[t] ^= 1;
             tc_fence_after();
+            {
+              // V^T: K-major (keys contiguous), 64-key boxes of D rows;
+              // V: MN-major (d contiguous), 16 keys = 2048 bytes per step
+              const uint64_t v0 = kVt ? sdesc_sw128(v_addr, 16, 1024)
+                                      : sdesc_sw128(v_addr, 128 * 128, 1024);
+              const uint32_t acc0 = j > 0 ? 1u : 0u;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
-                     sdesc_sw128(v_addr + kk * 2048, 128 * 128, 1024), kIdO,
-                     (j > 0 || kk > 0) ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tmem + 256 + t * 128, tmem + t * 128 + kk * 8,
+                       v0 + (kVt ? kmajor_step(kk, D) : mnmajor_step(kk)), kIdO,
+                       kk > 0 ? 1u : acc0);
             }
             mma_commit(&sm.o_full[t]);
           }
@@ -503,16 +518,25 @@ template <int D>
 int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
                     const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                     int causal, float scale, const lsx_tensor& o,
-                    const lsx_tensor& lse, int accumulate,
+                    const lsx_tensor& lse, int accumulate, void* vt,
                     const DeviceCtx& ctx, cudaStream_t s) {
   CUtensorMap tq, tk, tv;
   if (!make_map_bf16_4d(&tq, q.data, q.B, q.H, q.N, q.D, q.stride_b, q.stride_h,
                         q.stride_n, 128) ||
       !make_map_bf16_4d(&tk, k.data, k.B, k.H, k.N, k.D, k.stride_b, k.stride_h,
-                        k.stride_n, 128) ||
-      !make_map_bf16_4d(&tv, v.data, v.B, v.H, v.N, v.D, v.stride_b, v.stride_h,
-                        v.stride_n, 128))
+                        k.stride_n, 128))
     return LSX_ERR_LAUNCH;
+  if (vt != nullptr) {
+    // V^T [B, Hkv, D, Np]: rows are d, the inner (contiguous) axis is keys
+    const int rc = launch_transpose(v, vt, s);
+    if (rc != LSX_OK) return rc;
+    const int64_t np = transposed_row_len(v.N);
+    if (!make_map_bf16_4d(&tv, vt, v.B, v.H, v.D, v.N, v.H * v.D * np, v.D * np, np, D))
+      return LSX_ERR_LAUNCH;
+  } else if (!make_map_bf16_4d(&tv, v.data, v.B, v.H, v.N, v.D, v.stride_b, v.stride_h,
+                               v.stride_n, 128)) {
+    return LSX_ERR_LAUNCH;
+  }
   FwdParams p;
   p.B = q.B; p.Hq = q.H; p.Hkv = k.H; p.Lq = q.N; p.Lk = k.N;
   p.q_off = q_off; p.kv_off = kv_off;
@@ -526,30 +550,32 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
   p.l_sb = lse.stride_b; p.l_sh = lse.stride_h; p.l_sn = lse.stride_n;
   p.status = ctx.status; p.wait_ns = ctx.wait_ns;
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  if (cudaFuncSetAttribute(fwd_tc_kernel<D>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+  auto kern = vt != nullptr ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return LSX_ERR_LAUNCH;
   const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
   timing_begin(kKidFwdTc, s);
-  fwd_tc_kernel<D><<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, p);
+  kern<<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, p);
   timing_end(kKidFwdTc, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
 
 }  // namespace
 
+size_t fwd_tc_workspace_bytes(const lsx_tensor& v) { return transposed_bytes(v); }
+
 int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
-                  const lsx_tensor& lse, int accumulate, const DeviceCtx& ctx,
-                  cudaStream_t s) {
+                  const lsx_tensor& lse, int accumulate, void* vt,
+                  const DeviceCtx& ctx, cudaStream_t s) {
   if (q.D == 128)
     return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                                accumulate, ctx, s);
+                                accumulate, vt, ctx, s);
   if (q.D == 64)
     return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                               accumulate, ctx, s);
+                               accumulate, vt, ctx, s);
   return LSX_ERR_UNSUPPORTED;
 }
 

@@ -23,8 +23,14 @@ int device_ctx(DeviceCtx* ctx);
 // recorded on the launching stream around every launch of kernel `kid`.
 enum KernelId {
   kKidFwdTc = 0, kKidDkdv, kKidDq, kKidRowDot, kKidMerge, kKidTreeMerge,
-  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidCount
+  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidTranspose, kKidCount
 };
+
+// Sequence-contiguous copies (layout.cu): a bf16 [B, H, N, D] view is
+// written densely as [B, H, D, Np], Np = N rounded up to a multiple of 8.
+int64_t transposed_row_len(int64_t n);
+size_t transposed_bytes(const lsx_tensor& t);
+int launch_transpose(const lsx_tensor& in, void* out, cudaStream_t s);
 void timing_begin(int kid, cudaStream_t s);
 void timing_end(int kid, cudaStream_t s);
 
@@ -78,21 +84,32 @@ int launch_simt_bwd(const lsx_tensor& q, const lsx_tensor& k,
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
                     cudaStream_t s);
 
-// tcgen05 tensor-core forward (bf16 inputs).
+// tcgen05 tensor-core forward (bf16 inputs).  vt: NULL (V read as stored,
+// d-contiguous) or fwd_tc_workspace_bytes(v) of scratch that receives a
+// key-contiguous copy of V first, which the P.V product reads faster.
+size_t fwd_tc_workspace_bytes(const lsx_tensor& v);
 int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
-                  const lsx_tensor& lse, int accumulate, const DeviceCtx& ctx,
-                  cudaStream_t s);
+                  const lsx_tensor& lse, int accumulate, void* vt,
+                  const DeviceCtx& ctx, cudaStream_t s);
 
-// tcgen05 tensor-core backward (bf16 inputs).
+// tcgen05 tensor-core backward (bf16 inputs).  With copies.kt non-NULL, a
+// key-contiguous copy of K is written there first and the dQ product reads
+// it K-major; with NULL the K tiles are read as stored (MN-major), which
+// needs no scratch beyond delta.
+struct BwdCopies {
+  void* kt = nullptr;
+};
+size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k);
+BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base);
 int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, const lsx_tensor& lse,
-                  const lsx_tensor& d_o, const float* delta, int64_t q_off,
-                  int64_t kv_off, int causal, float scale,
-                  const lsx_tensor& dq, const lsx_tensor& dk,
-                  const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
-                  cudaStream_t s);
+                  const lsx_tensor& d_o, const float* delta,
+                  const BwdCopies& copies, int64_t q_off, int64_t kv_off,
+                  int causal, float scale, const lsx_tensor& dq,
+                  const lsx_tensor& dk, const lsx_tensor& dv, int accumulate,
+                  const DeviceCtx& ctx, cudaStream_t s);
 
 // Split-KV decode partials (bf16 inputs, D = 128).
 int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,

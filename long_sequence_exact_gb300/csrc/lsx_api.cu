@@ -35,7 +35,7 @@ std::vector<DevCache> g_devs;
 // ------------------------------------------------------- kernel timing
 const char* const kKernelNames[kKidCount] = {
     "fwd_tc", "bwd_dkdv_tc", "bwd_dq_tc", "bwd_row_dot", "merge", "tree_merge",
-    "decode_partials", "simt_fwd", "simt_bwd", "fill"};
+    "decode_partials", "simt_fwd", "simt_bwd", "fill", "transpose"};
 std::atomic<bool> g_timing{false};
 struct TimedLaunch {
   int kid;
@@ -266,13 +266,16 @@ int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
 }
 
 // -------------------------------------------------------- attn_chunk_fwd
+size_t attn_chunk_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+  if (q == nullptr || k == nullptr || q->dtype != LSX_BF16) return 0;
+  return fwd_tc_workspace_bytes(*k) + 256;
+}
+
 int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
                    const lsx_tensor* v, int64_t q_off, int64_t kv_off,
                    int causal, float scale, const lsx_tensor* o,
                    const lsx_tensor* lse, int accumulate, void* workspace,
                    size_t workspace_bytes, lsx_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
   LSX_TRY(check_qkv(q, k, v));
   LSX_TRY(check_view(o));
   if (o->B != q->B || o->H != q->H || o->N != q->N || o->D != q->D) return LSX_ERR_SHAPE;
@@ -280,6 +283,13 @@ int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
   LSX_TRY(check_row_aligned(o));
   LSX_TRY(check_lse(lse, q));
   if (q_off < 0 || kv_off < 0) return LSX_ERR_SHAPE;
+  // optional workspace: NULL, or large enough for the transposed copy of V
+  void* vt = nullptr;
+  if (workspace != nullptr && q->dtype == LSX_BF16) {
+    if (workspace_bytes < attn_chunk_fwd_workspace_size(q, k)) return LSX_ERR_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+    vt = workspace;
+  }
   DeviceCtx ctx;
   LSX_TRY(device_ctx(&ctx));
   const float sc = resolve_scale(scale, q->D);
@@ -290,15 +300,22 @@ int attn_chunk_fwd(const lsx_tensor* q, const lsx_tensor* k,
     return launch_simt_fwd(*q, *k, *v, q_off, kv_off, causal != 0, sc, *o, *lse,
                            accumulate != 0, ctx, s);
   return launch_fwd_tc(*q, *k, *v, q_off, kv_off, causal != 0, sc, *o, *lse,
-                       accumulate != 0, ctx, s);
+                       accumulate != 0, vt, ctx, s);
 }
 
 // -------------------------------------------------------- attn_chunk_bwd
-size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+size_t attn_chunk_bwd_min_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
   (void)k;
   if (q == nullptr) return 0;
   const int64_t rows = q->B * q->H * q->N;
-  return static_cast<size_t>(rows > 0 ? rows : 0) * sizeof(float) + 256;
+  return (static_cast<size_t>(rows > 0 ? rows : 0) * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+  if (q == nullptr || k == nullptr) return 0;
+  size_t n = attn_chunk_bwd_min_workspace_size(q, k);
+  if (q->dtype == LSX_BF16) n += bwd_tc_copies_bytes(*q, *k);
+  return n;
 }
 
 int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
@@ -329,9 +346,13 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
   LSX_TRY(check_row_aligned(dv));
   LSX_TRY(check_lse(lse, q));
   if (q_off < 0 || kv_off < 0) return LSX_ERR_SHAPE;
-  const size_t need = attn_chunk_bwd_workspace_size(q, k);
+  const size_t need = attn_chunk_bwd_min_workspace_size(q, k);
   if (workspace == nullptr || workspace_bytes < need) return LSX_ERR_WORKSPACE;
   if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  // room for the sequence-contiguous copies: the faster operand layout
+  BwdCopies copies;
+  if (q->dtype == LSX_BF16 && workspace_bytes >= attn_chunk_bwd_workspace_size(q, k))
+    copies = bwd_tc_copies(*q, *k, static_cast<char*>(workspace) + need);
   DeviceCtx ctx;
   LSX_TRY(device_ctx(&ctx));
   const float sc = resolve_scale(scale, q->D);
@@ -350,15 +371,15 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
   if (q->dtype == LSX_F32)
     return launch_simt_bwd(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off,
                            causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
-  return launch_bwd_tc(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off, causal != 0,
-                       sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
+  return launch_bwd_tc(*q, *k, *v, *lse, *d_o, delta, copies, q_off, kv_off,
+                       causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
 }
 
 // ------------------------------------------- whole-sequence chunked calls
 size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal) {
-  (void)q; (void)k; (void)chunk_len; (void)causal;
-  return 0;
+  (void)chunk_len; (void)causal;
+  return attn_chunk_fwd_workspace_size(q, k);
 }
 
 int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,

@@ -151,6 +151,20 @@ LSX_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Start-address offset (in the descriptor's 16-byte units) of K step kk of
+// a K-major SW128 operand whose rows span `rows` 128-byte lines per 64-column
+// box: 4 steps of 32 bytes inside a box, then the next box.  Adding it to a
+// base descriptor never carries out of the 14-bit address field because
+// shared memory addresses stay below 256 KB.
+__host__ __device__ constexpr uint64_t kmajor_step(int kk, int rows) {
+  return static_cast<uint64_t>(((kk / 4) * rows * 128 + (kk % 4) * 32) >> 4);
+}
+// Same for an MN-major operand whose K steps are 16 consecutive 128-byte
+// rows (2048 bytes).
+__host__ __device__ constexpr uint64_t mnmajor_step(int kk) {
+  return static_cast<uint64_t>((kk * 2048) >> 4);
+}
+
 // Instruction descriptor of tcgen05.mma.kind::f16: bf16 x bf16 -> f32.
 // a_mn / b_mn select MN-major (1) instead of K-major (0) operands.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn,

@@ -88,8 +88,10 @@ def test_fwd_rejects_bad_arguments_before_any_launch(lib):
 
 def test_bwd_requires_workspace(lib):
     q, k, v, o, l, do, dq, dk, dv = (_t(), _t(), _t(), _t(), _lse(), _t(), _t(), _t(), _t())
-    need = lib.attn_chunk_bwd_workspace_size(R(q), R(k))
+    need = lib.attn_chunk_bwd_min_workspace_size(R(q), R(k))
     assert need >= 2 * 128 * 4
+    # the full size adds the key-contiguous copy of K (2 heads x 128 x 128 bf16)
+    assert lib.attn_chunk_bwd_workspace_size(R(q), R(k)) >= need + 2 * 128 * 128 * 2
     rc = lib.attn_chunk_bwd(R(q), R(k), R(v), R(o), R(l), R(do), 0, 0, 1, -1.0, R(dq), R(dk),
                             R(dv), 0, None, 0, None)
     assert rc == -6

@@ -46,12 +46,14 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
-def test_chunk_bwd_matches_oracle(case, grad_dtype):
+@pytest.mark.parametrize("copies", [True, False], ids=["operand_copies", "as_stored"])
+def test_chunk_bwd_matches_oracle(case, grad_dtype, copies):
     b, hq, hkv, lq, lk, d, q_off, kv_off, causal = case
     q, k, v, d_o = make(b, hq, hkv, lq, lk, d, seed=lq + 7 * lk)
     # the saved O and LSE come from the GPU forward (as in training)
     o, lse = lsx.chunk_fwd(q, k, v, q_off, kv_off, causal)
-    grads = lsx.chunk_bwd(q, k, v, o, lse, d_o, q_off, kv_off, causal, grad_dtype=grad_dtype)
+    grads = lsx.chunk_bwd(q, k, v, o, lse, d_o, q_off, kv_off, causal, grad_dtype=grad_dtype,
+                          use_copies=copies)
     torch.cuda.synchronize()
     assert lsx.sync_status() == 0
     ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), q_off, kv_off, causal)
@@ -87,3 +89,13 @@ def test_backward_is_deterministic():
     b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_operand_layouts_give_the_same_gradients():
+    q, k, v, d_o = make(1, 4, 2, 640, 900, 128, seed=12)
+    o, lse = lsx.chunk_fwd(q, k, v, 300, 0, True)
+    a = lsx.chunk_bwd(q, k, v, o, lse, d_o, 300, 0, True, grad_dtype=torch.float32)
+    b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 300, 0, True, grad_dtype=torch.float32,
+                      use_copies=False)
+    for x, y in zip(a, b):
+        assert float((x - y).abs().max()) <= 1e-4 * max(1.0, float(y.abs().max()))

@@ -38,10 +38,12 @@ CASES = [
 
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("out_dtype", [torch.bfloat16, torch.float32])
-def test_chunk_fwd_matches_oracle(case, out_dtype):
+@pytest.mark.parametrize("v_copy", [True, False], ids=["v_transposed", "v_as_stored"])
+def test_chunk_fwd_matches_oracle(case, out_dtype, v_copy):
     b, hq, hkv, lq, lk, d, q_off, kv_off, causal = case
     q, k, v = qkv(b, hq, hkv, lq, lk, d, seed=11 + lq + lk)
-    o, lse = lsx.chunk_fwd(q, k, v, q_off, kv_off, causal, out_dtype=out_dtype)
+    o, lse = lsx.chunk_fwd(q, k, v, q_off, kv_off, causal, out_dtype=out_dtype,
+                           use_workspace=v_copy)
     torch.cuda.synchronize()
     assert lsx.sync_status() == 0
     o_ref, lse_ref = A.attn_fwd(f64(q), f64(k), f64(v), q_off, kv_off, causal)
@@ -105,3 +107,11 @@ def test_empty_key_chunk_gives_identity():
     k = torch.empty((1, 2, 0, 128), dtype=torch.bfloat16, device=DEV)
     o, lse = lsx.chunk_fwd(q, k, k, 0, 0, False, out_dtype=torch.float32)
     assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+
+
+def test_v_layouts_give_the_same_result():
+    q, k, v = qkv(2, 4, 2, 700, 900, 128, seed=8)
+    a = lsx.chunk_fwd(q, k, v, 200, 0, True, out_dtype=torch.float32, use_workspace=True)
+    b = lsx.chunk_fwd(q, k, v, 200, 0, True, out_dtype=torch.float32, use_workspace=False)
+    assert float((a[0] - b[0]).abs().max()) <= 1e-5
+    assert float((a[1] - b[1]).abs().max()) <= 1e-5
