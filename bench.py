@@ -267,6 +267,11 @@ def run_ours(args, rank, world, local_rank):
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         cpu = cpu_baseline(args.cpu_rows)
+    sec = None
+    if not args.no_secondary:
+        del q, k, v, d_o, o, lse, dq, dk, dv, ws, ws_f, x
+        torch.cuda.empty_cache()
+        sec = secondary(dev, pk)
 
     return {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -278,10 +283,82 @@ def run_ours(args, rank, world, local_rank):
                    "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd,
                    "l2": "inputs larger than L2 (q, k, v, dO 1 GiB each; no flush needed)",
                    "pct_of_tensor_peak": round(100.0 * value / world / pk["bf16_sustained"], 2)},
-        "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "kernels": kernels, "secondary": sec, "cpu_baseline": cpu,
+        "e2e": e2e,
         "gpu_launches": sum(c for c, _ in ktimes.values()),
         "clocks": clk.summary(),
     }
+
+
+# ----------------------------------------------- bandwidth-bound rows
+def secondary(dev, pk):
+    """HBM-bound rows of the path, timed alone with CUDA events (median of 5
+    after 3 warm-ups; every input is larger than L2):
+      merge       attn_merge of two fp32 partials at the 128K row count
+                  (B=1, H=32, N=131072, d=128): reads 2 x (O + LSE), writes 1
+      tree_merge  attn_tree_merge of 8 fp32 partials at the 32K row count
+      decode      attn_decode, B=8, Hq=32, Hkv=8, one query, 1,048,576-key
+                  cache, chunks of 4096 (partials + tree merge); algorithmic
+                  bytes = the K and V caches once + q + o
+    """
+    import torch
+    import long_sequence_exact_gb300 as lsx
+    from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs, random_tensor
+
+    def timed(fn, reps=5):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    out = {}
+    peak = pk["hbm_gbs"]
+    # pairwise merge
+    shape = (1, 32, 131072, 128)
+    oa = random_tensor(shape, 1, dtype=torch.float32, device=dev)
+    ob = random_tensor(shape, 2, dtype=torch.float32, device=dev)
+    la = random_tensor(shape[:3], 3, 5.0, dtype=torch.float32, device=dev)
+    lb = random_tensor(shape[:3], 4, 5.0, dtype=torch.float32, device=dev)
+    oo, lo = torch.empty_like(oa), torch.empty_like(la)
+    ms = timed(lambda: lsx.merge(oa, la, ob, lb, out=oo, lse_out=lo))
+    nbytes = 3 * (oa.numel() * 4 + la.numel() * 4)
+    out["merge"] = {"gbs": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 4),
+                    "ms": round(ms, 4), "bytes": nbytes}
+    del oa, ob, la, lb, oo, lo
+    # tree merge of 8 partials
+    k = 8
+    op = random_tensor((k, 1, 32, 32768, 128), 5, dtype=torch.float32, device=dev)
+    lp = random_tensor((k, 1, 32, 32768), 6, 5.0, dtype=torch.float32, device=dev)
+    to, tl = torch.empty(op.shape[1:], device=dev), torch.empty(lp.shape[1:], device=dev)
+    ms = timed(lambda: lsx.tree_merge(op, lp, out=to, lse_out=tl))
+    nbytes = (k + 1) * (to.numel() * 4 + tl.numel() * 4)
+    out["tree_merge"] = {"gbs": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 4),
+                         "ms": round(ms, 4), "bytes": nbytes, "k": k}
+    del op, lp, to, tl
+    # split-KV decode at 1M keys
+    w = WORKLOADS["decode_gqa_1m"]
+    x = make_inputs(w, device=dev, with_grad=False)
+    q, kc, vc = x["q"], x["k"], x["v"]
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ws = torch.empty(lsx.decode_workspace_size(q, kc, w.chunk), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: lsx.decode(q, kc, vc, w.chunk, out=o, lse=lse, workspace=ws))
+    nbytes = kc.numel() * 2 + vc.numel() * 2 + q.numel() * 2 + o.numel() * 2 + lse.numel() * 4
+    out["decode"] = {"gbs": round(nbytes / ms / 1e6, 1), "frac": round(nbytes / ms / 1e6 / peak, 4),
+                     "ms": round(ms, 4), "bytes": nbytes,
+                     "workload": "B=8 Hq=32 Hkv=8 N=1048576 d=128 chunk=4096"}
+    del x, q, kc, vc, o, lse, ws
+    torch.cuda.empty_cache()
+    out["peak_gbs"] = peak
+    out["peak_kind"] = f"{pk['source']} HBM copy bandwidth"
+    return out
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -349,6 +426,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the merge / tree-merge / decode bandwidth rows")
     ap.add_argument("--traffic", type=float, default=None,
                     help="dram bytes per launch of the dominant kernel from an ncu capture")
     ap.add_argument("--n", type=int, default=None,

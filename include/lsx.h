@@ -20,7 +20,8 @@
  * Conventions shared by every entry point
  *  - Tensors are rank-4 views [B, H, N, D] described by lsx_tensor.  The D
  *    axis is contiguous (stride 1); the other strides are in ELEMENTS.  A
- *    log-sum-exp tensor is a view with D == 1 (its stride_n must be 1).
+ *    log-sum-exp tensor is an fp32 view with D == 1, 4-byte aligned, with
+ *    any non-negative B/H/N strides (its stride along D is never used).
  *  - Every buffer is owned by the caller.  The library allocates no device or
  *    host memory; scratch space ("workspace") is passed in by the caller, who
  *    sizes it with the matching *_workspace_size call.  A workspace may be
@@ -151,11 +152,15 @@ int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
  * accumulate == 1: the contribution is added to the outputs (use f32
  *   outputs to sum over many chunk pairs).
  * Workspace (256-byte aligned): at least attn_chunk_bwd_min_workspace_size
- * bytes (the row sums delta_i = <dO_i, O_i>).  With
- * attn_chunk_bwd_workspace_size bytes (bf16 inputs), sequence-contiguous
- * copies of Q, dO and K are also written there and the dV, dK, dQ products
- * read them at the tensor cores' faster operand layout; with less, the
- * tiles are read as stored.  Both give the same results.
+ * bytes (the row sums delta_i = <dO_i, O_i>, 4 bytes per query row).  With
+ * attn_chunk_bwd_workspace_size bytes (bf16 inputs) two more things are
+ * written there first: a key-contiguous copy of K, which the dQ product
+ * reads at the tensor cores' faster operand layout, and 16 bytes per query
+ * row of row statistics (-LSE/scale and -delta as bf16 triples), which the
+ * dK/dV kernel adds to its score products on the tensor cores instead of
+ * per element.  With less, K is read as stored and the statistics are
+ * applied per element.  Both give results within the documented tolerance
+ * of each other (the statistics triples carry 24 significant bits).
  * ---------------------------------------------------------------------- */
 size_t attn_chunk_bwd_min_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
 size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);

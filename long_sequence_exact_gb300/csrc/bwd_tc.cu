@@ -162,9 +162,11 @@ struct DkdvSmem {
   __nv_bfloat16 v[128 * D];
   __nv_bfloat16 q[2][128 * D];
   __nv_bfloat16 d_o[2][128 * D];
+  __nv_bfloat16 rs[2][128 * 8];   // row statistics of Q_i (core-matrix order)
+  __nv_bfloat16 ones[2][128 * 8]; // selector tiles for -LSE/scale and -delta
   float lse2[2][128];             // LSE * log2(e); +inf for rows without keys
   float delta[2][128];
-  uint64_t kv_full, kv_empty, final_bar;
+  uint64_t kv_full, kv_empty, final_bar, ones_full;
   uint64_t st_full[2], st_empty[2];
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_full, p_full, dkv_done;
@@ -232,12 +234,20 @@ __host__ __device__ constexpr uint64_t seq_b_step(int kk) {
   return kTransposed ? kmajor_step(kk, D) : mnmajor_step(kk);
 }
 
-template <int D>
+// With kRS the score products carry the row statistics themselves: after
+// the D/16 K steps of K Q_i^T (or V dO_i^T) one more K step multiplies a
+// selector tile by the statistics tile of Q_i, which adds -LSE/scale (or
+// -delta) to every score of each query column; the grad warps then need
+// neither the LSE nor delta.  Without kRS warp 0 gathers both into shared
+// memory and the grad warps apply them per element.
+template <int D, bool kRS>
 __global__ void __launch_bounds__(640, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v,
-                const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_do,
+                const __grid_constant__ CUtensorMap tm_rs,
+                const __grid_constant__ CUtensorMap tm_ones, const BwdParams p) {
   using Sm = DkdvSmem<D>;
   constexpr int kTile = 128 * D * 2;
   constexpr int kQoStages = 2;
@@ -251,6 +261,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.kv_full, 1);
     mbar_init(&sm.kv_empty, 1);
     mbar_init(&sm.final_bar, 1);
+    mbar_init(&sm.ones_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.st_full[s], 1);
       mbar_init(&sm.st_empty[s], 1);
@@ -280,6 +291,11 @@ __global__ void __launch_bounds__(640, 1)
     if (warp == 0) {
       // -------------------------------------------------- loads (warp 0)
       uint32_t qs = 0, qph = 0, ls = 0, lph = 0, kv_phase = 0;
+      if (kRS && lane == 0) {
+        mbar_arrive_expect_tx(&sm.ones_full, 2 * 128 * 16);
+        tma_load_4d(sm.ones[0], &tm_ones, &sm.ones_full, 0, 0, 0, 0);
+        tma_load_4d(sm.ones[1], &tm_ones, &sm.ones_full, 0, 128, 0, 0);
+      }
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
@@ -298,11 +314,15 @@ __global__ void __launch_bounds__(640, 1)
           // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV)
           if (!mbar_wait(&sm.st_empty[qs], qph ^ 1, guard)) { ok = false; break; }
           if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.st_full[qs], 2 * kTile);
+            mbar_arrive_expect_tx(&sm.st_full[qs], 2 * kTile + (kRS ? 128 * 16 : 0));
             load_tile<D, false>(sm.q[qs], &tm_q, &sm.st_full[qs], i * 128, h, x.b);
             load_tile<D, false>(sm.d_o[qs], &tm_do, &sm.st_full[qs], i * 128, h, x.b);
+            if constexpr (kRS)
+              tma_load_4d(sm.rs[qs], &tm_rs, &sm.st_full[qs], 0, static_cast<int>(i * 128),
+                          static_cast<int>(h), static_cast<int>(x.b));
           }
           if (++qs == kQoStages) { qs = 0; qph ^= 1; }
+          if constexpr (kRS) continue;
           // LSE (log2 units) and delta of the 128 query rows of tile i
           if (!mbar_wait(&sm.lse_empty[ls], lph ^ 1, guard)) { ok = false; break; }
           for (int t = lane; t < 128; t += 32) {
@@ -328,7 +348,14 @@ __global__ void __launch_bounds__(640, 1)
       uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0;
       bool issued = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
-      for (int64_t r = 0;; ++r) {
+      // selector and statistics tiles: 16 core matrices of 8 rows x 16 bytes
+      // along M/N (128 bytes apart); the K step's second core matrix re-reads
+      // the first (distance 0 along K), which the halved statistics undo.
+      const uint64_t sel_c = sdesc_interleave(smem_addr(sm.ones[0]), 0, 128);
+      const uint64_t sel_d = sdesc_interleave(smem_addr(sm.ones[1]), 0, 128);
+      bool ones_ok = true;
+      if constexpr (kRS) ones_ok = mbar_wait(&sm.ones_full, 0, guard);
+      for (int64_t r = 0; ones_ok; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
         const DkdvItem x = dkdv_item(p, it);
@@ -342,7 +369,14 @@ __global__ void __launch_bounds__(640, 1)
           const uint32_t q_addr = smem_addr(sm.q[qs]);
           const uint32_t o_addr = smem_addr(sm.d_o[qs]);
           mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
-          mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+          if constexpr (kRS) {
+            const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
+            mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
+            mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+            mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
+          } else {
+            mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+          }
           mma_commit(&sm.s_full);
           issued = true;
           if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
@@ -395,7 +429,7 @@ __global__ void __launch_bounds__(640, 1)
         const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
-        if (!mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
+        if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
         tc_fence_after();
         uint32_t us[32], ud[32];
         ld_two(tS, tP, us, ud);
@@ -408,7 +442,25 @@ __global__ void __launch_bounds__(640, 1)
         }
         const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[ls][32 * qtr]);
         const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[ls][32 * qtr]);
-        {
+        if constexpr (kRS) {
+          // the scores already hold S - LSE/scale and dP - delta
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c0 = 2 * e;
+            const float2 arg = __fmul2_rn(
+                make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2);
+            float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+            if (c0 < cmin) pr.x = 0.f;
+            if (c0 + 1 < cmin) pr.y = 0.f;
+            const float2 ds = __fmul2_rn(
+                pr, make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])));
+            pk[e] = pack_bf16(pr.x, pr.y);
+            dk[e] = pack_bf16(ds.x, ds.y);
+          }
+          tmem_st16(tS, pk);
+          tmem_st16(tP, dk);
+        } else {
           constexpr int cc = 0;
           uint32_t pk[16], dk[16];
 #pragma unroll
@@ -435,9 +487,9 @@ __global__ void __launch_bounds__(640, 1)
           }
           tmem_st16(tS + cc * 16, pk);
           tmem_st16(tP + cc * 16, dk);
+          mbar_arrive(&sm.lse_empty[ls]);
+          if (++ls == 2) { ls = 0; lph ^= 1; }
         }
-        mbar_arrive(&sm.lse_empty[ls]);
-        if (++ls == 2) { ls = 0; lph ^= 1; }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full);
@@ -791,6 +843,10 @@ bool map_transposed(CUtensorMap* m, const lsx_tensor& t, void* copy, int box_row
   return make_map_bf16_4d(m, copy, t.B, t.H, t.D, t.N, t.H * t.D * np, t.D * np, np, box_rows);
 }
 
+bool map_ones(CUtensorMap* m, void* ones) {
+  return make_map_bf16_rows8(m, ones, 1, 1, 256);
+}
+
 template <int D>
 int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                     const lsx_tensor& lse, const lsx_tensor& d_o, const float* delta,
@@ -799,7 +855,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
                     cudaStream_t s) {
   const bool tr = cp.kt != nullptr;
-  CUtensorMap tq, tk, tv, tdo, tkt;
+  const bool rs = cp.stats.rows != nullptr;
+  CUtensorMap tq, tk, tv, tdo, tkt, trs, tones;
   if (!map_rows(&tq, q) || !map_rows(&tk, k) || !map_rows(&tv, v) || !map_rows(&tdo, d_o))
     return LSX_ERR_LAUNCH;
   if (tr) {
@@ -808,6 +865,14 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
     if (!map_transposed(&tkt, k, cp.kt, D)) return LSX_ERR_LAUNCH;
   } else {
     tkt = tk;
+  }
+  if (rs) {
+    if (!make_map_bf16_rows8(&trs, cp.stats.rows, q.B, q.H, q.N) ||
+        !map_ones(&tones, cp.stats.ones))
+      return LSX_ERR_LAUNCH;
+  } else {
+    trs = tk;
+    tones = tk;
   }
   BwdParams p;
   p.B = q.B; p.Hq = q.H; p.Hkv = k.H; p.Lq = q.N; p.Lk = k.N;
@@ -830,13 +895,13 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.n_items = p.n_ktiles * q.B * k.H;
   {
     const size_t smem = sizeof(DkdvSmem<D>) + 1024;
-    auto kern = dkdv_kernel<D>;
+    auto kern = rs ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDkdv, s);
-    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, p);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, p);
     timing_end(kKidDkdv, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
@@ -859,16 +924,21 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
 
 }  // namespace
 
+// Scratch behind delta: [key-contiguous K][selector tiles, 4 KiB][row
+// statistics, 16 bytes per query row].
 size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k) {
-  (void)q;
-  return (transposed_bytes(k) + 255) / 256 * 256;
+  const size_t kt = (transposed_bytes(k) + 255) / 256 * 256;
+  const size_t rows = static_cast<size_t>(q.B * q.H * q.N);
+  return kt + (2 * 128 * 16 + rows * 16 + 255) / 256 * 256;
 }
 
 BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base) {
   (void)q;
-  (void)k;
   BwdCopies c;
   c.kt = base;
+  char* st = static_cast<char*>(base) + (transposed_bytes(k) + 255) / 256 * 256;
+  c.stats.ones = st;
+  c.stats.rows = st + 2 * 128 * 16;
   return c;
 }
 

@@ -59,7 +59,14 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
                       cudaStream_t s);
 
 // delta[b,h,n] = <dO[b,h,n,:], O[b,h,n,:]> into a dense f32 [B*H*N] buffer.
+// With rows non-NULL it also writes the per-row statistics operand of the
+// tensor-core dK/dV kernel (see RowStats) from the same row and lse.
+struct RowStats {
+  void* rows = nullptr;  // bf16 [B*H*N][8]
+  void* ones = nullptr;  // bf16 [2][128][8] selector tiles
+};
 int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
+                   const RowStats& stats, const lsx_tensor* lse, float scale,
                    const DeviceCtx& ctx, cudaStream_t s);
 
 // Writes O = 0 and LSE = -inf for every row (a pair with no visible key);
@@ -97,9 +104,13 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
 // tcgen05 tensor-core backward (bf16 inputs).  With copies.kt non-NULL, a
 // key-contiguous copy of K is written there first and the dQ product reads
 // it K-major; with NULL the K tiles are read as stored (MN-major), which
-// needs no scratch beyond delta.
+// needs no scratch beyond delta.  With copies.stats.rows non-NULL (written
+// by launch_row_dot beforehand) the dK/dV kernel takes -LSE/scale and
+// -delta into its score products as one extra rank-1 K step instead of
+// applying them per element.
 struct BwdCopies {
   void* kt = nullptr;
+  RowStats stats;
 };
 size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k);
 BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base);

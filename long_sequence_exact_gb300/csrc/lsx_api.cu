@@ -367,7 +367,7 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
     return LSX_OK;
   }
   float* delta = static_cast<float*>(workspace);
-  LSX_TRY(launch_row_dot(*o, *d_o, delta, ctx, s));
+  LSX_TRY(launch_row_dot(*o, *d_o, delta, copies.stats, lse, sc, ctx, s));
   if (q->dtype == LSX_F32)
     return launch_simt_bwd(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off,
                            causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);

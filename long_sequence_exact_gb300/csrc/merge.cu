@@ -244,15 +244,55 @@ __global__ void __launch_bounds__(256) tree_merge_block_kernel(
 }
 
 // ----------------------------------------------------------- row dot
+// bf16 bits of x rounded to nearest, and the f32 remainder x - that value
+// (exact: the remainder of a round to 8 significant bits fits in f32).
+__device__ __forceinline__ uint32_t bf16_split(float x, float& rem) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(x);
+  rem = x - __bfloat162float(h);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(h));
+}
+
+// Row statistics operand of the tensor-core dK/dV kernel, one 16-byte row per
+// query row: bf16 {c1, c2, c3, d1, d2, d3, 0, 0} with c1 + c2 + c3 = c / 2,
+// c = -LSE / scale (c = -2^100 when LSE = -inf, so that the row's
+// probabilities underflow to 0), and d1 + d2 + d3 = -delta / 2: each value
+// is carried by three bf16 terms (24 significant bits).  The halving is
+// undone by the kernel, which reads the 8 stored columns twice in its K step
+// of 16.  Selector tiles: rows of {1, 1, 1, 0, 0, 0, 0, 0} (tile 0) and
+// {0, 0, 0, 1, 1, 1, 0, 0} (tile 1), so that a K step of
+// (selector x statistics^T) adds c or -delta to every score of a query
+// column.
+__device__ __forceinline__ uint4 row_stats(float lse, float delta, float inv_scale) {
+  const float c = lse == kNegInf ? -0x1p100f : -lse * inv_scale;
+  float r;
+  const uint32_t c1 = bf16_split(0.5f * c, r);
+  const uint32_t c2 = bf16_split(r, r);
+  const uint32_t c3 = bf16_split(r, r);
+  const uint32_t d1 = bf16_split(-0.5f * delta, r);
+  const uint32_t d2 = bf16_split(r, r);
+  const uint32_t d3 = bf16_split(r, r);
+  return make_uint4(c1 | (c2 << 16), c3 | (d1 << 16), d2 | (d3 << 16), 0u);
+}
+
 template <int E>
 __global__ void __launch_bounds__(256) row_dot_kernel(lsx_tensor o,
                                                       lsx_tensor d_o,
                                                       float* delta,
-                                                      int64_t rows) {
+                                                      int64_t rows,
+                                                      uint4* stats,
+                                                      uint4* ones,
+                                                      lsx_tensor lse,
+                                                      float inv_scale) {
   const int lane = threadIdx.x & 31;
   const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   const RowIdx ri{o.H, o.N};
+  if (ones != nullptr && blockIdx.x == 0) {
+    const uint32_t one = 0x3F80u;  // bf16 1.0
+    ones[threadIdx.x] = threadIdx.x < 128
+                            ? make_uint4(one | (one << 16), one, 0u, 0u)
+                            : make_uint4(0u, one << 16, one | (one << 16), 0u);
+  }
   for (int64_t row = w0; row < rows; row += nw) {
     int64_t b, h, n;
     ri.split(row, b, h, n);
@@ -261,7 +301,12 @@ __global__ void __launch_bounds__(256) row_dot_kernel(lsx_tensor o,
     float s = 0.f;
     for (int e = 0; e < E; ++e) s = fmaf(x.v[e], y.v[e], s);
     for (int k = 16; k > 0; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
-    if (lane == 0) delta[row] = s;
+    if (lane == 0) {
+      delta[row] = s;
+      if (stats != nullptr)
+        stats[row] = row_stats(static_cast<const float*>(lse.data)[view_off(lse, b, h, n)], s,
+                               inv_scale);
+    }
   }
 }
 
@@ -335,12 +380,22 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
 }
 
 int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
+                   const RowStats& stats, const lsx_tensor* lse, float scale,
                    const DeviceCtx& ctx, cudaStream_t s) {
   const int64_t rows = o.B * o.H * o.N;
   if (rows == 0) return LSX_OK;
   const int grid = grid_for_rows(rows, ctx, 8);
+  uint4* st = static_cast<uint4*>(stats.rows);
+  uint4* on = static_cast<uint4*>(stats.ones);
+  lsx_tensor l{};
+  if (st != nullptr) {
+    if (lse == nullptr || on == nullptr) return LSX_ERR_LAUNCH;
+    l = *lse;
+  }
+  const float inv_scale = static_cast<float>(1.0 / static_cast<double>(scale));
   timing_begin(kKidRowDot, s);
-  LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid, 256, 0, s>>>(o, d_o, delta, rows));
+  LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid, 256, 0, s>>>(o, d_o, delta, rows, st, on, l,
+                                                             inv_scale));
   timing_end(kKidRowDot, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }

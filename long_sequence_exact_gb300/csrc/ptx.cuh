@@ -151,6 +151,19 @@ LSX_DEV uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return d;
 }
 
+// Shared-memory matrix descriptor without swizzling: the operand is stored
+// as 8-row x 16-byte core matrices of 128 contiguous bytes; lbo is the byte
+// distance between core matrices adjacent along K, sbo between those adjacent
+// along M/N.
+LSX_DEV uint64_t sdesc_interleave(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  return d;
+}
+
 // Start-address offset (in the descriptor's 16-byte units) of K step kk of
 // a K-major SW128 operand whose rows span `rows` 128-byte lines per 64-column
 // box: 4 steps of 32 bytes inside a box, then the next box.  Adding it to a

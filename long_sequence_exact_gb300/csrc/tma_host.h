@@ -52,4 +52,23 @@ inline bool make_map_bf16_4d(CUtensorMap* map, const void* base, int64_t B,
   return r == CUDA_SUCCESS;
 }
 
+// Tiled map over a dense bf16 array [B][H][N][8] (16 bytes per row), box
+// {8, 128, 1, 1} without swizzle: one box is 128 rows of 16 bytes, i.e. 16
+// consecutive 8 x 16-byte core matrices.  Rows beyond N read as zero.
+inline bool make_map_bf16_rows8(CUtensorMap* map, const void* base, int64_t B,
+                                int64_t H, int64_t N) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {8u, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {16u, (cuuint64_t)(N * 16), (cuuint64_t)(H * N * 16)};
+  cuuint32_t box[4] = {8u, 128u, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                   const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace lsx

