@@ -180,9 +180,9 @@ struct DkdvItem {
 
 __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
   DkdvItem x;
-  const int64_t bh_n = p.B * p.Hkv;
-  x.j = it / bh_n;  // key tile 0 (the most query tiles) first
-  const int64_t bh = it % bh_n;
+  int64_t rank, bh;
+  banded_item(it, p.n_ktiles, p.B * p.Hkv, &rank, &bh);
+  x.j = rank;  // key tile 0 (the most query tiles) first
   x.b = bh / p.Hkv;
   x.hk = bh % p.Hkv;
   x.group = p.Hq / p.Hkv;
@@ -566,9 +566,9 @@ struct DqItem {
 
 __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int64_t it) {
   DqItem x;
-  const int64_t bh_n = p.B * p.Hq;
-  x.i = p.n_qtiles - 1 - it / bh_n;  // the longest key range first
-  const int64_t bh = it % bh_n;
+  int64_t rank, bh;
+  banded_item(it, p.n_qtiles, p.B * p.Hq, &rank, &bh);
+  x.i = p.n_qtiles - 1 - rank;  // the longest key range first
   x.b = bh / p.Hq;
   x.h = bh % p.Hq;
   x.hk = x.h / (p.Hq / p.Hkv);

@@ -98,9 +98,9 @@ struct Item {
 
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
   Item x;
-  const int64_t bh_n = p.B * p.Hq;
-  x.pair = p.n_qpairs - 1 - it / bh_n;
-  const int64_t bh = it % bh_n;
+  int64_t rank, bh;
+  banded_item(it, p.n_qpairs, p.B * p.Hq, &rank, &bh);
+  x.pair = p.n_qpairs - 1 - rank;
   x.b = bh / p.Hq;
   x.h = bh % p.Hq;
   x.hk = x.h / (p.Hq / p.Hkv);

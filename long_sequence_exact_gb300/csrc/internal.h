@@ -152,10 +152,38 @@ __host__ __device__ inline int64_t fwd_kv_tiles(int64_t t, int64_t Lq,
   return kmax > 0 ? (kmax + 127) / 128 : 0;
 }
 
-// Work item -> (bh, pair) for the persistent forward grid.  Items are in
-// decreasing-cost order (the pair with the most key tiles first); CTA c of G
-// takes, in round r, item r*G + c on even rounds and r*G + (G-1-c) on odd
-// rounds (a "snake" deal that evens out the longest-first order).
+// Work item -> (rank, bh) for the persistent grids.  The units of one
+// (batch, head) pair -- query tiles or key tiles -- are ranked by cost, rank 0
+// being the most expensive.  Items are grouped in bands of band_width ranks:
+// band 0 holds ranks [0, W) of every (b, h), (b, h) by (b, h), then band 1,
+// and so on.  Neighbouring items, which run at the same time on neighbouring
+// CTAs, then share a head and stream the same K/V (or Q/dO) tiles, so most
+// tile loads hit L2; and the bands still run from the most expensive ranks
+// to the cheapest, which the longest-first deal below relies on.  Small
+// problems (fewer than 256 units) use W = 1: plain longest-first order.
+__host__ __device__ inline int64_t band_width(int64_t n_units) {
+  return n_units >= 256 ? 64 : 1;
+}
+__host__ __device__ inline void banded_item(int64_t it, int64_t n_units, int64_t bh_n,
+                                            int64_t* rank, int64_t* bh) {
+  const int64_t w = band_width(n_units);
+  const int64_t full = n_units / w;  // complete bands
+  const int64_t per_band = w * bh_n;
+  if (it < full * per_band) {
+    const int64_t k = it % per_band;
+    *bh = k / w;
+    *rank = (it / per_band) * w + k % w;
+  } else {
+    const int64_t k = it - full * per_band;
+    const int64_t tail = n_units - full * w;
+    *bh = k / tail;
+    *rank = full * w + k % tail;
+  }
+}
+
+// Item index for CTA c of G in round r.  Items are in (banded) decreasing-
+// cost order; CTA c takes item r*G + c on even rounds and r*G + (G-1-c) on
+// odd rounds (a "snake" deal that evens out the longest-first order).
 __host__ __device__ inline int64_t snake_item(int64_t c, int64_t r, int64_t G) {
   return r * G + ((r & 1) ? (G - 1 - c) : c);
 }

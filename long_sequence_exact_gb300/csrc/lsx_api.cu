@@ -524,7 +524,9 @@ int lsx_schedule_stats(int64_t B, int64_t H, int64_t N, int64_t chunk_len,
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= n_items) break;
-      const int64_t pair = n_qpairs - 1 - it / (B * H);
+      int64_t rank, bh;
+      banded_item(it, n_qpairs, B * H, &rank, &bh);
+      const int64_t pair = n_qpairs - 1 - rank;
       const int64_t a = fwd_kv_tiles(2 * pair, N, N, 0, 0, causal);
       const int64_t b = fwd_kv_tiles(2 * pair + 1, N, N, 0, 0, causal);
       const int64_t cost = a + b;  // one S and one P.V product per tile row
