@@ -38,6 +38,14 @@ UNIT = "TFLOP/s"
 WORKLOAD = "causal_128k_balanced"
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
+# tensor-core kernel on the 128K workload, from one single-pass ncu capture of
+# this bench (--steps 1 --warmup 1).  They describe the kernels as they were
+# captured and are re-taken whenever a kernel changes.
+DRAM_BYTES_128K = {"fwd_tc": 36.22e9 + 1.39e9, "bwd_dkdv_tc": 28.17e9 + 2.13e9,
+                   "bwd_dq_tc": 79.21e9 + 1.08e9}
+
+
 def flops(b, h, n, d, causal=True):
     pairs = n * (n + 1) / 2 if causal else n * n
     fwd = 4.0 * b * h * pairs * d
@@ -256,12 +264,18 @@ def run_ours(args, rank, world, local_rank):
             ent["achieved_tflops"] = round(ach, 1)
             ent["frac_of_peak"] = round(ach / pk["bf16_sustained"], 4)
         kernels[name] = ent
+    for name in kernels:
+        if workload == WORKLOAD and name in DRAM_BYTES_128K:
+            kernels[name]["dram_bytes_per_launch"] = DRAM_BYTES_128K[name]
     if dom is not None and dom[0] in algo:
+        traffic = args.traffic
+        if traffic is None and workload == WORKLOAD:
+            traffic = DRAM_BYTES_128K.get(dom[0])
         name, (cnt, tot) = dom
         ach = algo[name] / (tot / cnt / 1e3) / 1e12
         roofline = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
-                    "frac": round(ach / pk["bf16_sustained"], 4), "traffic": args.traffic,
+                    "frac": round(ach / pk["bf16_sustained"], 4), "traffic": traffic,
                     "peak_kind": f"{pk['source']} bf16 sustained (kernel timed inside a long step)"}
 
     cpu = None
@@ -397,12 +411,14 @@ def run_reference(args, rank):
     if rank != 0:
         return None
     cores = len(os.sched_getaffinity(0))
+    # each reference step is a quarter of the main arm's sample (a few
+    # seconds), so that --steps K --warmup W ends within minutes
     for _ in range(args.warmup):
-        cpu_baseline(args.cpu_rows // 4)
+        cpu_baseline(max(1, args.cpu_rows // 16))
     vals = []
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        vals.append(cpu_baseline(args.cpu_rows))
+        vals.append(cpu_baseline(max(1, args.cpu_rows // 4)))
     total = time.perf_counter() - t0
     value = statistics.mean(v["value"] for v in vals)
     return {
@@ -423,7 +439,8 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=3072,
+                    help="query rows in the oracle's CPU sample (about 10 s on 16 cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
