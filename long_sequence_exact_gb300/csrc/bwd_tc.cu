@@ -151,6 +151,53 @@ __device__ __forceinline__ void ld_two(uint32_t ta, uint32_t tb, uint32_t (&a)[3
   reg_fence32(b);
 }
 
+// P^T and dS^T of one grad thread's 32 scores when the score products
+// already hold S - LSE/scale and dP - delta; with kMask, the query columns
+// c < cmin (not yet visible to this key) get P = 0.
+template <bool kMask>
+__device__ __forceinline__ void grad_rows_rs(const uint32_t (&us)[32], const uint32_t (&ud)[32],
+                                             float2 sc2, int cmin, uint32_t (&pk)[16],
+                                             uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int c0 = 2 * e;
+    const float2 arg = __fmul2_rn(
+        make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2);
+    float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+    if (kMask) {
+      if (c0 < cmin) pr.x = 0.f;
+      if (c0 + 1 < cmin) pr.y = 0.f;
+    }
+    const float2 ds =
+        __fmul2_rn(pr, make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])));
+    pk[e] = pack_bf16(pr.x, pr.y);
+    dk[e] = pack_bf16(ds.x, ds.y);
+  }
+}
+
+// dS of one dQ grad thread's 32 scores; with kMask, key columns c > climit
+// (not visible to this query, or past the keys) get P = 0.
+template <bool kMask>
+__device__ __forceinline__ void grad_cols_dq(const uint32_t (&us)[32], const uint32_t (&ud)[32],
+                                             float2 sc2, float2 nl, float2 nd, int climit,
+                                             uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const int c0 = 2 * e;
+    const float2 arg = __ffma2_rn(
+        make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
+    float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+    if (kMask) {
+      if (c0 > climit) pr.x = 0.f;
+      if (c0 + 1 > climit) pr.y = 0.f;
+    }
+    const float2 dpm = __fadd2_rn(
+        make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
+    const float2 ds = __fmul2_rn(pr, dpm);
+    dk[e] = pack_bf16(ds.x, ds.y);
+  }
+}
+
 // ===================================================================== dK dV
 // The dV / dK products read dO and Q as stored (MN-major B operands, the
 // same tiles the S^T / dP^T products use): measured faster here than
@@ -443,21 +490,15 @@ __global__ void __launch_bounds__(640, 1)
         const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[ls][32 * qtr]);
         const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[ls][32 * qtr]);
         if constexpr (kRS) {
-          // the scores already hold S - LSE/scale and dP - delta
+          // the scores already hold S - LSE/scale and dP - delta; only
+          // tiles that straddle the diagonal for this warp need the mask
+          const bool need_mask =
+              p.causal && p.kv_off + x.j * 128 + quad * 32 + 31 > p.q_off + i * 128 + 32 * qtr;
           uint32_t pk[16], dk[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c0 = 2 * e;
-            const float2 arg = __fmul2_rn(
-                make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2);
-            float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
-            if (c0 < cmin) pr.x = 0.f;
-            if (c0 + 1 < cmin) pr.y = 0.f;
-            const float2 ds = __fmul2_rn(
-                pr, make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])));
-            pk[e] = pack_bf16(pr.x, pr.y);
-            dk[e] = pack_bf16(ds.x, ds.y);
-          }
+          if (need_mask)
+            grad_rows_rs<true>(us, ud, sc2, cmin, pk, dk);
+          else
+            grad_rows_rs<false>(us, ud, sc2, cmin, pk, dk);
           tmem_st16(tS, pk);
           tmem_st16(tP, dk);
         } else {
@@ -782,20 +823,15 @@ __global__ void __launch_bounds__(640, 1)
           if (c2 < lim) lim = c2;
         }
         const int climit = lim < -1 ? -1 : static_cast<int>(lim);
+        // every column visible to every row of this warp: no mask needed
+        const bool need_mask =
+            kb + 32 > p.Lk ||
+            (p.causal && p.q_off + x.i * 128 + quad * 32 - p.kv_off - kb < 31);
         uint32_t dk[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = 2 * e;
-          const float2 arg = __ffma2_rn(
-              make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
-          float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
-          if (c0 > climit) pr.x = 0.f;
-          if (c0 + 1 > climit) pr.y = 0.f;
-          const float2 dpm = __fadd2_rn(
-              make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
-          const float2 ds = __fmul2_rn(pr, dpm);
-          dk[e] = pack_bf16(ds.x, ds.y);
-        }
+        if (need_mask)
+          grad_cols_dq<true>(us, ud, sc2, nl, nd, climit, dk);
+        else
+          grad_cols_dq<false>(us, ud, sc2, nl, nd, climit, dk);
         // the dS columns are free once the previous dQ product has read them
         if (n_ds > 0) {
           if (!mbar_wait(&sm.ds_free, (n_ds - 1) & 1, guard)) { ok = false; break; }
