@@ -8,18 +8,28 @@
 // per key/value head (the G query heads of a group share it), so the
 // algorithmic traffic is the cache size.
 //
-// Decomposition: one CTA of 8 warps per (batch, kv head, chunk).  A warp
+// Decomposition: one CTA of 8 compute warps per (batch, kv head, chunk).  A warp
 // takes 32/G consecutive keys per step (G = query heads per kv head), lane l
 // holding elements [4l, 4l+4) of every row, so each row is one coalesced
 // 256-byte access.  The G x (32/G) partial dot products are folded with a
 // 31-shuffle transpose-reduce that leaves score (key l / G, head l % G) in
 // lane l.  Each warp keeps an online softmax per head; the 8 warp states are
 // merged in shared memory at the end with the LSE rule.
+//
+// Two forms of the same arithmetic:
+//  * decode_tma_kernel (G = 2, 4, 8): a ninth warp streams the chunk through a
+//    ring of shared-memory stages with TMA (one stage = one key block per
+//    compute warp, K and V), so that tens of kilobytes per SM are in flight
+//    while the compute warps reduce; the compute warps read rows from shared
+//    memory.
+//  * decode_partials_kernel (any G, and any layout the TMA maps reject):
+//    each warp loads its rows into registers itself.
 #include <cuda_bf16.h>
 #include <math.h>
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tma_host.h"
 
 namespace lsx {
 namespace {
@@ -39,6 +49,8 @@ struct DecodeParams {
   float scale_log2;
   float* part_o;
   float* part_l;
+  int* status;
+  uint64_t wait_ns;
 };
 
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
@@ -172,13 +184,217 @@ __global__ void __launch_bounds__(256) decode_partials_kernel(DecodeParams p) {
   }
 }
 
+template <int G>
+struct DecodeTmaCfg {
+  static constexpr int kKpi = 32 / G;               // keys per warp per stage
+  static constexpr int kKeys = kWarps * kKpi;       // keys per stage
+  static constexpr int kStages = G == 2 ? 2 : (G == 4 ? 3 : 4);
+  static constexpr int kBox = kKeys * 128;          // one [kKeys][64] bf16 box
+  static constexpr int kStageBytes = 4 * kBox;      // K and V, two boxes each
+  static constexpr int kSmem = kStages * kStageBytes + 256;
+};
+
+// Row r, elements [4 lane, 4 lane + 4) of a stage tile stored as two
+// [kKeys][64] boxes (columns 0..63, then 64..127).
+__device__ __forceinline__ void row4(const uint8_t* tile, int box_bytes, int r, int lane,
+                                     float (&x)[4]) {
+  const uint2 u = *reinterpret_cast<const uint2*>(tile + (lane >> 4) * box_bytes + r * 128 +
+                                                  (lane & 15) * 8);
+  const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(&u.x);
+  const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&u.y);
+  x[0] = __low2float(a); x[1] = __high2float(a);
+  x[2] = __low2float(b); x[3] = __high2float(b);
+}
+
+template <int G>
+__global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
+    decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  using C = DecodeTmaCfg<G>;
+  constexpr int KPI = C::kKpi;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                               ~uintptr_t(127));
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
+  __shared__ float s_m[kWarps][G];
+  __shared__ float s_l[kWarps][G];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int64_t k0 = chunk * p.chunk_len;
+  const int64_t k1 = (k0 + p.chunk_len < p.N) ? k0 + p.chunk_len : p.N;
+  const int64_t n_steps = (k1 - k0 + C::kKeys - 1) / C::kKeys;
+  const WaitGuard guard{p.status, p.wait_ns, abort_flag};
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  float m = kNegInf, l = 0.f;  // state of head (lane % G)
+  float o[G][4];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[g][e] = 0.f;
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int64_t s = 0; s < n_steps; ++s) {
+        const int stg = static_cast<int>(s % C::kStages);
+        const uint32_t round = static_cast<uint32_t>(s / C::kStages);
+        if (round > 0 && !mbar_wait(&empty[stg], (round & 1) ^ 1, guard)) break;
+        uint8_t* dst = stages + stg * C::kStageBytes;
+        const int row = static_cast<int>(k0 + s * C::kKeys);
+        mbar_arrive_expect_tx(&full[stg], C::kStageBytes);
+        for (int half = 0; half < 2; ++half) {
+          tma_load_4d(dst + half * C::kBox, &tm_k, &full[stg], half * 64, row,
+                      static_cast<int>(hk), static_cast<int>(b));
+          tma_load_4d(dst + (2 + half) * C::kBox, &tm_v, &full[stg], half * 64, row,
+                      static_cast<int>(hk), static_cast<int>(b));
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- compute warps
+    float qv[G][4];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      load4(p.q + b * p.q_sb + (hk * G + g) * p.q_sh + lane * 4, qv[g]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) qv[g][e] *= p.scale_log2;
+    }
+    for (int64_t s = 0; s < n_steps; ++s) {
+      const int stg = static_cast<int>(s % C::kStages);
+      if (!mbar_wait(&full[stg], static_cast<uint32_t>(s / C::kStages) & 1, guard)) break;
+      const uint8_t* kt = stages + stg * C::kStageBytes;
+      const uint8_t* vt = kt + 2 * C::kBox;
+      const int64_t base = k0 + s * C::kKeys + warp * KPI;
+      // partial dots, index i = kk * G + g
+      float part[32];
+#pragma unroll
+      for (int kk = 0; kk < KPI; ++kk) {
+        float kr[4];
+        row4(kt, C::kBox, warp * KPI + kk, lane, kr);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a = fmaf(qv[g][e], kr[e], a);
+          part[kk * G + g] = a;
+        }
+      }
+      // transpose-reduce: afterwards part[0] = full sum of index `lane`
+#pragma unroll
+      for (int half = 16; half >= 1; half >>= 1) {
+        const bool up = (lane & half) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? part[i] : part[i + half];
+          const float keep = up ? part[i + half] : part[i];
+          part[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+        }
+      }
+      float sc = part[0];
+      if (base + lane / G >= k1) sc = kNegInf;  // past the chunk (zero-filled rows)
+      float mx = sc;
+#pragma unroll
+      for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float m_new = fmaxf(m, mx);
+      const float alpha = (m == kNegInf) ? 0.f : ex2(m - m_new);
+      const float mu = (m_new == kNegInf) ? 0.f : m_new;
+      const float pr = ex2(sc - mu);
+      float ps = pr;
+#pragma unroll
+      for (int off = G; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      l = l * alpha + ps;
+      m = m_new;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float ag = __shfl_sync(0xffffffffu, alpha, g);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[g][e] *= ag;
+      }
+#pragma unroll
+      for (int kk = 0; kk < KPI; ++kk) {
+        float vr[4];
+        row4(vt, C::kBox, warp * KPI + kk, lane, vr);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float pkg = __shfl_sync(0xffffffffu, pr, kk * G + g);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) o[g][e] = fmaf(pkg, vr[e], o[g][e]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stg]);  // this warp is done with the stage
+    }
+  }
+  // merge the warps' states; the per-warp O rows reuse the stage memory once
+  // every stage has been consumed
+  __syncthreads();
+  float* s_o = reinterpret_cast<float*>(stages);  // [kWarps][G][128]
+  if (warp < kWarps) {
+    if (lane < G) {
+      s_m[warp][lane] = m;
+      s_l[warp][lane] = l;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s_o[(warp * G + g) * 128 + lane * 4 + e] = o[g][e];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * 128; idx += blockDim.x) {
+    const int g = idx / 128, d = idx % 128;
+    float mm = kNegInf;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_m[w][g]);
+    float tot = 0.f, acc = 0.f;
+    if (mm != kNegInf) {
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float f = (s_m[w][g] == kNegInf) ? 0.f : ex2(s_m[w][g] - mm);
+        tot += s_l[w][g] * f;
+        acc += s_o[(w * G + g) * 128 + d] * f;
+      }
+    }
+    const int64_t row = b * p.Hq + hk * G + g;
+    p.part_o[(chunk * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
+    if (d == 0)
+      p.part_l[chunk * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
+  }
+}
+
+template <int G>
+bool launch_decode_tma(const lsx_tensor& kc, const lsx_tensor& vc, const DecodeParams& p,
+                       dim3 grid, cudaStream_t s) {
+  using C = DecodeTmaCfg<G>;
+  CUtensorMap tk, tv;
+  if (!make_map_bf16_4d(&tk, kc.data, kc.B, kc.H, kc.N, kc.D, kc.stride_b, kc.stride_h,
+                        kc.stride_n, C::kKeys, false) ||
+      !make_map_bf16_4d(&tv, vc.data, vc.B, vc.H, vc.N, vc.D, vc.stride_b, vc.stride_h,
+                        vc.stride_n, C::kKeys, false))
+    return false;  // layout the TMA cannot describe: the register kernel runs
+  if (cudaFuncSetAttribute(decode_tma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmem) != cudaSuccess)
+    return false;
+  decode_tma_kernel<G><<<grid, 32 * (kWarps + 1), C::kSmem, s>>>(tk, tv, p);
+  return true;
+}
+
 }  // namespace
 
 int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
                            const lsx_tensor& vc, int64_t chunk_len,
                            float scale, float* part_o, float* part_lse,
                            const DeviceCtx& ctx, cudaStream_t s) {
-  (void)ctx;
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q.data);
   p.q_sb = q.stride_b; p.q_sh = q.stride_h;
@@ -190,12 +406,20 @@ int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
   p.rows = q.B * q.H;
   p.scale_log2 = scale * kLog2e;
   p.part_o = part_o; p.part_l = part_lse;
+  p.status = ctx.status; p.wait_ns = ctx.wait_ns;
   const int64_t parts = ceil_div(kc.N, chunk_len);
   if (parts > 65535 * 1024LL || kc.H > 65535 || q.B > 65535) return LSX_ERR_UNSUPPORTED;
   dim3 grid(static_cast<unsigned>(parts), static_cast<unsigned>(kc.H),
             static_cast<unsigned>(q.B));
   timing_begin(kKidDecode, s);
+  bool done = false;
   switch (q.H / kc.H) {
+    case 2: done = launch_decode_tma<2>(kc, vc, p, grid, s); break;
+    case 4: done = launch_decode_tma<4>(kc, vc, p, grid, s); break;
+    case 8: done = launch_decode_tma<8>(kc, vc, p, grid, s); break;
+    default: break;
+  }
+  if (!done) switch (q.H / kc.H) {
     case 1: decode_partials_kernel<1><<<grid, 256, 0, s>>>(p); break;
     case 2: decode_partials_kernel<2><<<grid, 256, 0, s>>>(p); break;
     case 4: decode_partials_kernel<4><<<grid, 256, 0, s>>>(p); break;

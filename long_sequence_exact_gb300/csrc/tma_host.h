@@ -27,11 +27,13 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // Tiled map over a bf16 tensor with dims (innermost first) {D, N, H, B} and
 // element strides {1, sn, sh, sb}.  Box = {64, box_rows, 1, 1} with the
 // 128-byte swizzle, so one box is box_rows rows of 128 bytes, matching the
-// K-major / MN-major SW128 shared-memory layouts the MMAs read.  Rows beyond
-// N read as zero.  Returns false when the driver rejects the map.
+// K-major / MN-major SW128 shared-memory layouts the MMAs read (or, with
+// swizzle = false, plain row-major [box_rows][64]).  Rows beyond N read as
+// zero.  Returns false when the driver rejects the map.
 inline bool make_map_bf16_4d(CUtensorMap* map, const void* base, int64_t B,
                              int64_t H, int64_t N, int64_t D, int64_t sb,
-                             int64_t sh, int64_t sn, uint32_t box_rows) {
+                             int64_t sh, int64_t sn, uint32_t box_rows,
+                             bool swizzle = true) {
   auto enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   // a stride of an extent-1 dimension is never used; give it a legal value
@@ -46,7 +48,8 @@ inline bool make_map_bf16_4d(CUtensorMap* map, const void* base, int64_t B,
   cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                    const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -109,7 +109,7 @@ def test_fp32_tiny_workload_chunks_merge_and_backward():
     check_close(f64(dv), dv_r, TOL_FP32, "dV")
 
 
-@pytest.mark.parametrize("g", [1, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
 def test_decode_matches_oracle(g):
     hkv, n, chunk = 2, 20000, 4096  # ragged last chunk
     q = random_tensor((2, hkv * g, 1, 128), 30, device=DEV)
