@@ -106,6 +106,23 @@ struct RowIdx {
 
 // ------------------------------------------------------------ pairwise
 template <int E>
+__device__ __forceinline__ void merge_one(const Vec<E>& va, const Vec<E>& vb, float xa, float xb,
+                                          Vec<E>& out, float& l) {
+  const float m = fmaxf(xa, xb);
+  if (m == kNegInf) {
+    for (int e = 0; e < E; ++e) out.v[e] = 0.f;
+    l = kNegInf;
+  } else {
+    const float wa = expf(xa - m), wb = expf(xb - m);
+    const float tot = wa + wb;
+    const float ra = wa / tot, rb = wb / tot;
+    for (int e = 0; e < E; ++e) out.v[e] = ra * va.v[e] + rb * vb.v[e];
+    l = m + logf(tot);
+  }
+}
+
+// One warp per row.
+template <int E>
 __global__ void __launch_bounds__(256) merge_kernel(
     lsx_tensor oa, lsx_tensor la, lsx_tensor ob, lsx_tensor lb, lsx_tensor oo,
     lsx_tensor lo, int64_t rows) {
@@ -123,19 +140,9 @@ __global__ void __launch_bounds__(256) merge_kernel(
     const float xb = plb[view_off(lb, b, h, n)];
     const Vec<E> va = load_row<E>(oa.data, oa.dtype, view_off(oa, b, h, n), lane);
     const Vec<E> vb = load_row<E>(ob.data, ob.dtype, view_off(ob, b, h, n), lane);
-    const float m = fmaxf(xa, xb);
     Vec<E> out;
     float l;
-    if (m == kNegInf) {
-      for (int e = 0; e < E; ++e) out.v[e] = 0.f;
-      l = kNegInf;
-    } else {
-      const float wa = expf(xa - m), wb = expf(xb - m);
-      const float tot = wa + wb;
-      const float ra = wa / tot, rb = wb / tot;
-      for (int e = 0; e < E; ++e) out.v[e] = ra * va.v[e] + rb * vb.v[e];
-      l = m + logf(tot);
-    }
+    merge_one<E>(va, vb, xa, xb, out, l);
     // all lanes have read their inputs before any store (outputs may alias)
     __syncwarp();
     store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, out);
@@ -144,8 +151,9 @@ __global__ void __launch_bounds__(256) merge_kernel(
 }
 
 // ------------------------------------------------------------- k-way
-// One warp per row; partials are taken in order p = 0, 1, ..., n-1 so the
-// result does not depend on the launch shape.
+// One warp per row (n_parts <= 32).  Lane p holds partial p's LSE; the
+// partial rows are read four at a time, loads first, and accumulated in the
+// order p = 0, 1, ..., n-1, so the result does not depend on the launch shape.
 template <int E>
 __global__ void __launch_bounds__(256) tree_merge_warp_kernel(
     lsx_tensor op, int64_t pso, lsx_tensor lp, int64_t psl, int n_parts,
@@ -160,18 +168,26 @@ __global__ void __launch_bounds__(256) tree_merge_warp_kernel(
     ri.split(row, b, h, n);
     const int64_t lbase = view_off(lp, b, h, n);
     const int64_t obase = view_off(op, b, h, n);
-    float m = kNegInf;
-    for (int p = lane; p < n_parts; p += 32) m = fmaxf(m, plp[lbase + p * psl]);
+    const float x = lane < n_parts ? plp[lbase + lane * psl] : kNegInf;
+    float m = x;
     for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    const float wl = (m == kNegInf || lane >= n_parts) ? 0.f : expf(x - m);
+    float tot = wl;
+    for (int s = 16; s > 0; s >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, s);
     Vec<E> acc;
     for (int e = 0; e < E; ++e) acc.v[e] = 0.f;
-    float tot = 0.f;
     if (m != kNegInf) {
-      for (int p = 0; p < n_parts; ++p) {
-        const float w = expf(plp[lbase + p * psl] - m);
-        const Vec<E> x = load_row<E>(op.data, op.dtype, obase + p * pso, lane);
-        tot += w;
-        for (int e = 0; e < E; ++e) acc.v[e] = fmaf(w, x.v[e], acc.v[e]);
+      for (int p0 = 0; p0 < n_parts; p0 += 4) {
+        Vec<E> xs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (p0 + u < n_parts) xs[u] = load_row<E>(op.data, op.dtype, obase + (p0 + u) * pso, lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, (p0 + u) & 31);
+          if (p0 + u < n_parts)
+            for (int e = 0; e < E; ++e) acc.v[e] = fmaf(w, xs[u].v[e], acc.v[e]);
+        }
       }
       const float inv = 1.f / tot;
       for (int e = 0; e < E; ++e) acc.v[e] *= inv;
