@@ -306,14 +306,20 @@ def run_ours(args, rank, world, local_rank):
 
 # ----------------------------------------------- bandwidth-bound rows
 def secondary(dev, pk):
-    """HBM-bound rows of the path, timed alone with CUDA events (median of 5
-    after 3 warm-ups; every input is larger than L2):
+    """Rows of the path other than the headline, timed alone with CUDA events
+    (median of 5 after 3 warm-ups; every input is larger than L2):
       merge       attn_merge of two fp32 partials at the 128K row count
                   (B=1, H=32, N=131072, d=128): reads 2 x (O + LSE), writes 1
       tree_merge  attn_tree_merge of 8 fp32 partials at the 32K row count
       decode      attn_decode, B=8, Hq=32, Hkv=8, one query, 1,048,576-key
                   cache, chunks of 4096 (partials + tree merge); algorithmic
                   bytes = the K and V caches once + q + o
+      causal_32k_ring, noncausal_64k_heavytail
+                  chunked fwd+bwd of the other two attention workloads
+                  (TFLOP/s against the sustained bf16 peak)
+      autograd_remat_32k
+                  backward time through torch.autograd with the checkpoint
+                  at the attention output vs at the layer input (re-run)
     """
     import torch
     import long_sequence_exact_gb300 as lsx
@@ -372,6 +378,59 @@ def secondary(dev, pk):
     torch.cuda.empty_cache()
     out["peak_gbs"] = peak
     out["peak_kind"] = f"{pk['source']} HBM copy bandwidth"
+    # fwd+bwd throughput of the other attention workloads (same flop
+    # convention: visible pairs only), against the sustained bf16 peak
+    for name, causal in (("causal_32k_ring", True), ("noncausal_64k_heavytail", False)):
+        w = WORKLOADS[name]
+        x = make_inputs(w, device=dev)
+        q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
+        o, lse = lsx.chunked_fwd(q, k, v, w.chunk, causal=causal)
+        grads = lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=causal)
+
+        def fwd_bwd():
+            lsx.chunked_fwd(q, k, v, w.chunk, causal=causal, out=o, lse=lse)
+            lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=causal, dq=grads[0],
+                            dk=grads[1], dv=grads[2])
+
+        ms = timed(fwd_bwd)
+        ff, fb = flops(w.B, w.Hq, w.N, w.D, causal)
+        tf = (ff + fb) / (ms / 1e3) / 1e12
+        out[name] = {"tflops": round(tf, 1), "frac": round(tf / pk["bf16_sustained"], 4),
+                     "ms": round(ms, 3), "flops": ff + fb,
+                     "workload": f"B={w.B} H={w.Hq} N={w.N} d={w.D} chunk={w.chunk} "
+                                 f"{'causal' if causal else 'non-causal'}"}
+        del x, q, k, v, d_o, o, lse, grads
+        torch.cuda.empty_cache()
+    out["tflops_peak"] = pk["bf16_sustained"]
+    # backward through torch.autograd with the checkpoint at the attention
+    # output (O, LSE kept) against the layer-boundary form (forward re-run)
+    w = WORKLOADS["causal_32k_ring"]
+    x = make_inputs(w, device=dev)
+    q, k, v = (x[n_].requires_grad_() for n_ in ("q", "k", "v"))
+    d_o = x["d_o"]
+    res = {}
+    for mode in ("output", "inputs"):
+        ts = []
+        for it in range(8):
+            o = lsx.chunked_attention(q, k, v, w.chunk, True, checkpoint=mode)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record()
+            o.backward(d_o)
+            b.record()
+            torch.cuda.synchronize()
+            if it >= 3:
+                ts.append(a.elapsed_time(b))
+            q.grad = k.grad = v.grad = None
+            del o
+        res[mode] = statistics.median(ts)
+    out["autograd_remat_32k"] = {
+        "bwd_ms_checkpoint_output": round(res["output"], 3),
+        "bwd_ms_checkpoint_inputs": round(res["inputs"], 3),
+        "speedup": round(res["inputs"] / res["output"], 3),
+        "workload": "causal_32k_ring through lsx.chunked_attention (torch.autograd)"}
+    del x, q, k, v, d_o
+    torch.cuda.empty_cache()
     return out
 
 

@@ -22,9 +22,11 @@ from .attention import (  # noqa: F401
     tree_merge,
     version,
 )
+from .autograd import ChunkedAttention, chunked_attention  # noqa: F401
 
 __all__ = [
     "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "merge", "tree_merge",
     "decode", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
-    "set_wait_limit_ns", "status_string", "sync_status", "version",
+    "set_wait_limit_ns", "status_string", "sync_status", "version", "chunked_attention",
+    "ChunkedAttention",
 ]

@@ -121,7 +121,8 @@ __device__ __forceinline__ void merge_one(const Vec<E>& va, const Vec<E>& vb, fl
   }
 }
 
-// One warp per row.
+// One warp per row (any layout and dtype; the dense fp32 case below is
+// faster).
 template <int E>
 __global__ void __launch_bounds__(256) merge_kernel(
     lsx_tensor oa, lsx_tensor la, lsx_tensor ob, lsx_tensor lb, lsx_tensor oo,
@@ -147,6 +148,52 @@ __global__ void __launch_bounds__(256) merge_kernel(
     __syncwarp();
     store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, out);
     if (lane == 0) plo[view_off(lo, b, h, n)] = l;
+  }
+}
+
+// Dense fp32 form (every O tensor [B, H, N, D] contiguous, LSE [B, H, N]
+// contiguous, the output LSE separate from the inputs'): a grid-stride loop
+// over 16-byte pieces, four per thread per iteration, each piece combined
+// with its row's two LSE values.  A thread writes only the pieces it read,
+// so the output O may be one of the inputs.
+__global__ void __launch_bounds__(256) merge_dense_kernel(
+    const float4* __restrict__ oa, const float* __restrict__ la, const float4* __restrict__ ob,
+    const float* __restrict__ lb, float4* oo, float* lo, int64_t n4, int d4) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4;
+       i0 += 4 * stride) {
+    float4 xa[4], xb[4];
+    float sa[4], sb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n4) {
+        const int64_t row = i / d4;
+        xa[u] = __ldcs(oa + i);
+        xb[u] = __ldcs(ob + i);
+        sa[u] = __ldg(la + row);
+        sb[u] = __ldg(lb + row);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = i0 + u * stride;
+      if (i < n4) {
+        const float m = fmaxf(sa[u], sb[u]);
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        float l = kNegInf;
+        if (m != kNegInf) {
+          const float wa = expf(sa[u] - m), wb = expf(sb[u] - m);
+          const float tot = wa + wb;
+          const float ra = wa / tot, rb = wb / tot;
+          r = make_float4(ra * xa[u].x + rb * xb[u].x, ra * xa[u].y + rb * xb[u].y,
+                          ra * xa[u].z + rb * xb[u].z, ra * xa[u].w + rb * xb[u].w);
+          l = m + logf(tot);
+        }
+        __stcs(oo + i, r);
+        if (i % d4 == 0) lo[i / d4] = l;
+      }
+    }
   }
 }
 
@@ -346,10 +393,33 @@ __global__ void __launch_bounds__(256) fill_kernel(lsx_tensor o,
   }
 }
 
-int grid_for_rows(int64_t rows, const DeviceCtx& ctx, int warps_per_block) {
-  const int64_t blocks = ceil_div(rows, warps_per_block);
-  const int64_t cap = static_cast<int64_t>(ctx.sm_count) * 8;  // 8 x 256 threads per SM
+// Grid of a row-loop kernel of 256-thread blocks: one block per `per_block`
+// rows, capped at the blocks the GPU holds at once (SMs x resident blocks per
+// SM for this kernel), so that every block is resident and the grid-stride
+// loops share the rows evenly instead of leaving a partial second wave.
+template <typename Kernel>
+int grid_for_rows(Kernel kernel, int64_t rows, const DeviceCtx& ctx, int64_t per_block) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 256, 0) != cudaSuccess ||
+      per_sm < 1)
+    per_sm = 1;
+  const int64_t blocks = ceil_div(rows, per_block);
+  const int64_t cap = static_cast<int64_t>(ctx.sm_count) * per_sm;
   return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+bool dense_rows(const lsx_tensor& t) {
+  return t.stride_n == t.D && t.stride_h == t.N * t.D && (t.B == 1 || t.stride_b == t.H * t.N * t.D);
+}
+bool dense_lse(const lsx_tensor& t) {
+  return t.stride_n == 1 && t.stride_h == t.N && (t.B == 1 || t.stride_b == t.H * t.N);
+}
+// Whether two dense [B, H, N, D] fp32 views share any byte.
+bool overlaps(const lsx_tensor& a, const lsx_tensor& b) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.data), b0 = reinterpret_cast<uintptr_t>(b.data);
+  const uintptr_t an = static_cast<uintptr_t>(a.B * a.H * a.N * a.D) * 4;
+  const uintptr_t bn = static_cast<uintptr_t>(b.B * b.H * b.N * b.D) * 4;
+  return a0 < b0 + bn && b0 < a0 + an;
 }
 
 }  // namespace
@@ -367,9 +437,31 @@ int launch_merge(const lsx_tensor& oa, const lsx_tensor& la,
                  const DeviceCtx& ctx, cudaStream_t s) {
   const int64_t rows = oa.B * oa.H * oa.N;
   if (rows == 0) return LSX_OK;
-  const int grid = grid_for_rows(rows, ctx, 8);
   timing_begin(kKidMerge, s);
-  LSX_DISPATCH_E(oa.D, merge_kernel<E><<<grid, 256, 0, s>>>(oa, la, ob, lb, oo, lo, rows));
+  const bool dense = oa.dtype == LSX_F32 && ob.dtype == LSX_F32 && oo.dtype == LSX_F32 &&
+                     dense_rows(oa) && dense_rows(ob) && dense_rows(oo) && dense_lse(la) &&
+                     dense_lse(lb) && dense_lse(lo) && oa.D % 4 == 0 &&
+                     (oo.data == oa.data || oo.data == ob.data ||
+                      (!overlaps(oo, oa) && !overlaps(oo, ob))) &&
+                     lo.data != la.data && lo.data != lb.data;
+  if (dense) {
+    const int64_t n4 = rows * oa.D / 4;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_dense_kernel, 256, 0) !=
+            cudaSuccess || per_sm < 1)
+      per_sm = 1;
+    const int64_t need = ceil_div(n4, 256 * 4);
+    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * per_sm;
+    merge_dense_kernel<<<static_cast<int>(need < cap ? need : cap), 256, 0, s>>>(
+        static_cast<const float4*>(oa.data), static_cast<const float*>(la.data),
+        static_cast<const float4*>(ob.data), static_cast<const float*>(lb.data),
+        static_cast<float4*>(oo.data), static_cast<float*>(lo.data), n4,
+        static_cast<int>(oa.D / 4));
+    timing_end(kKidMerge, s);
+    return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+  }
+  LSX_DISPATCH_E(oa.D, merge_kernel<E><<<grid_for_rows(merge_kernel<E>, rows, ctx, 8), 256, 0,
+                                          s>>>(oa, la, ob, lb, oo, lo, rows));
   timing_end(kKidMerge, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
@@ -382,13 +474,12 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
   if (rows == 0) return LSX_OK;
   timing_begin(kKidTreeMerge, s);
   if (n_parts <= 16) {
-    const int grid = grid_for_rows(rows, ctx, 8);
-    LSX_DISPATCH_E(op.D, tree_merge_warp_kernel<E><<<grid, 256, 0, s>>>(
+    LSX_DISPATCH_E(op.D, tree_merge_warp_kernel<E><<<
+                             grid_for_rows(tree_merge_warp_kernel<E>, rows, ctx, 8), 256, 0, s>>>(
                              op, pso, lp, psl, n_parts, oo, lo, rows));
   } else {
-    const int64_t cap = static_cast<int64_t>(ctx.sm_count) * 8;
-    const int grid = static_cast<int>(rows < cap ? rows : cap);
-    LSX_DISPATCH_E(op.D, tree_merge_block_kernel<E><<<grid, 256, 0, s>>>(
+    LSX_DISPATCH_E(op.D, tree_merge_block_kernel<E><<<
+                             grid_for_rows(tree_merge_block_kernel<E>, rows, ctx, 1), 256, 0, s>>>(
                              op, pso, lp, psl, n_parts, oo, lo, rows));
   }
   timing_end(kKidTreeMerge, s);
@@ -400,7 +491,6 @@ int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
                    const DeviceCtx& ctx, cudaStream_t s) {
   const int64_t rows = o.B * o.H * o.N;
   if (rows == 0) return LSX_OK;
-  const int grid = grid_for_rows(rows, ctx, 8);
   uint4* st = static_cast<uint4*>(stats.rows);
   uint4* on = static_cast<uint4*>(stats.ones);
   lsx_tensor l{};
@@ -410,8 +500,8 @@ int launch_row_dot(const lsx_tensor& o, const lsx_tensor& d_o, float* delta,
   }
   const float inv_scale = static_cast<float>(1.0 / static_cast<double>(scale));
   timing_begin(kKidRowDot, s);
-  LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid, 256, 0, s>>>(o, d_o, delta, rows, st, on, l,
-                                                             inv_scale));
+  LSX_DISPATCH_E(o.D, row_dot_kernel<E><<<grid_for_rows(row_dot_kernel<E>, rows, ctx, 8), 256, 0,
+                                            s>>>(o, d_o, delta, rows, st, on, l, inv_scale));
   timing_end(kKidRowDot, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
@@ -420,9 +510,9 @@ int launch_fill_empty(const lsx_tensor& o, const lsx_tensor& lse,
                       const DeviceCtx& ctx, cudaStream_t s) {
   const int64_t rows = o.B * o.H * o.N;
   if (rows == 0) return LSX_OK;
-  const int grid = grid_for_rows(rows, ctx, 8);
   timing_begin(kKidFill, s);
-  LSX_DISPATCH_E(o.D, fill_kernel<E><<<grid, 256, 0, s>>>(o, lse, rows));
+  LSX_DISPATCH_E(o.D, fill_kernel<E><<<grid_for_rows(fill_kernel<E>, rows, ctx, 8), 256, 0, s>>>(
+                          o, lse, rows));
   timing_end(kKidFill, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }

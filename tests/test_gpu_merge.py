@@ -51,6 +51,23 @@ def test_merge_in_place_and_extreme_gaps():
     check_close(f64(oa), ref[0], TOL_FP32)
 
 
+def test_merge_dense_and_strided_fp32_forms_agree():
+    # contiguous fp32 rows take the elementwise kernel (here with O in place),
+    # head-interleaved views the warp-per-row kernel
+    shape = (2, 4, 300, 128)
+    oa, la = partial(shape, 5, empty_rows=(3,))
+    ob, lb = partial(shape, 6, empty_rows=(3, 4))
+    ref = A.lse_merge(f64(oa), f64(la), f64(ob), f64(lb))
+    sa = oa.transpose(1, 2).contiguous().transpose(1, 2)  # [B, N, H, D] storage
+    sb = ob.transpose(1, 2).contiguous().transpose(1, 2)
+    o_s, l_s = lsx.merge(sa, la, sb, lb)
+    l_d = torch.empty_like(la)
+    lsx.merge(oa, la, ob, lb, out=oa, lse_out=l_d)
+    for o, l in ((oa, l_d), (o_s, l_s)):
+        check_lse(f64(l), ref[1], 1e-5)
+        check_close(f64(o), ref[0], TOL_FP32)
+
+
 @pytest.mark.parametrize("k_parts", [1, 2, 5, 16, 17, 256])
 def test_tree_merge_matches_oracle(k_parts):
     shape = (k_parts, 2, 4, 33, 128)
