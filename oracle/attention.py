@@ -34,6 +34,16 @@ What is computed, and where the pages fix it
   rebuilds the softmax rows from Q and K and applies the softmax Jacobian
   explicitly, dS_ij = P_ij * (dP_ij - sum_k P_ik dP_ik).
 
+* Block-sparse attention.  The Fine-grained Attention I/O Complexity page
+  (abstract) extends the analysis to sparse attention, and the related-work
+  list of the BriefGPT BurstAttention page names FlashAttention extended to
+  a broad class of sparsity patterns.  Neither fixes a mask format; reading
+  taken: a block mask over (query block, key block) of BLOCK x BLOCK
+  positions, counted from the start of the chunks, shared by every batch row
+  and head.  Key j is visible to query i iff the mask entry of their blocks
+  is set AND the causal rule (if any) holds; a query left with no visible
+  key gets O = 0, LSE = -inf as above.
+
 The rows are processed in blocks only to bound memory (the full score matrix
 of a 128K sequence is 128 GiB in fp64); each block holds complete score rows
 and applies the two-pass softmax, so the blocking changes nothing.
@@ -96,18 +106,30 @@ def _shapes(q, k, v):
     return b, hq, hkv, lq, lk, d
 
 
-def _scores(qh, kh, q_pos, k_pos, causal, scale):
+def block_visible(q_idx: np.ndarray, k_idx: np.ndarray, block_mask, block: int = 128):
+    """Boolean [len(q_idx), len(k_idx)]: the mask entry of block
+    (q // block, k // block) is set (indices from the start of the chunks)."""
+    m = np.asarray(block_mask) != 0
+    return m[np.asarray(q_idx)[:, None] // block, np.asarray(k_idx)[None, :] // block]
+
+
+def _scores(qh, kh, q_pos, k_pos, causal, scale, bvis=None):
     s = scale * (qh @ kh.T)
-    return np.where(visible(q_pos, k_pos, causal), s, NEG_INF)
+    vis = visible(q_pos, k_pos, causal)
+    if bvis is not None:
+        vis = vis & bvis
+    return np.where(vis, s, NEG_INF)
 
 
 def attn_fwd(q, k, v, q_off=0, kv_off=0, causal=False, scale=None,
-             rows=None, block=256):
+             rows=None, block=256, block_mask=None, mask_block=128):
     """Exact attention of a query chunk against a key/value chunk.
 
     q: [B, H_q, L_q, d]; k, v: [B, H_kv, L_k, d] (v may have its own last dim).
     q_off / kv_off: absolute position of row 0 of the chunk (causal mask only).
     rows: optional indices into L_q; only those query rows are computed.
+    block_mask: optional [ceil(L_q/mask_block), ceil(L_k/mask_block)] array;
+    only keys of set blocks are visible (see the module docstring).
     Returns (O [B, H_q, len(rows), d_v] float64, LSE [B, H_q, len(rows)]).
     """
     q = np.asarray(q, dtype=np.float64)
@@ -125,8 +147,10 @@ def attn_fwd(q, k, v, q_off=0, kv_off=0, causal=False, scale=None,
             g = kv_head_of(h, hq, hkv)
             for r0 in range(0, rows.shape[0], block):
                 ri = rows[r0:r0 + block]
+                bv = None if block_mask is None else block_visible(
+                    ri, np.arange(lk), block_mask, mask_block)
                 s = _scores(q[bi, h, ri], k[bi, g], q_off + ri, k_pos, causal,
-                            scale)
+                            scale, bv)
                 p, l_ = _softmax_rows(s)
                 out[bi, h, r0:r0 + ri.shape[0]] = p @ v[bi, g]
                 lse[bi, h, r0:r0 + ri.shape[0]] = l_
@@ -134,7 +158,7 @@ def attn_fwd(q, k, v, q_off=0, kv_off=0, causal=False, scale=None,
 
 
 def attn_bwd(q, k, v, d_o, q_off=0, kv_off=0, causal=False, scale=None,
-             rows=None, block=256):
+             rows=None, block=256, block_mask=None, mask_block=128):
     """Gradients of L = sum(d_o * O) with respect to q, k, v.
 
     Rebuilds each softmax row from q and k and applies the softmax Jacobian
@@ -165,8 +189,10 @@ def attn_bwd(q, k, v, d_o, q_off=0, kv_off=0, causal=False, scale=None,
             for r0 in range(0, rows.shape[0], block):
                 ri = rows[r0:r0 + block]
                 qh = q[bi, h, ri]
+                bv = None if block_mask is None else block_visible(
+                    ri, np.arange(lk), block_mask, mask_block)
                 p, _ = _softmax_rows(_scores(qh, kh, q_off + ri, k_pos, causal,
-                                             scale))
+                                             scale, bv))
                 doh = d_o[bi, h, ri]
                 dp = doh @ vh.T
                 ds = _apply_softmax_jacobian(p, dp)

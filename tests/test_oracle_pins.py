@@ -448,8 +448,8 @@ def test_planted_dropped_jacobian_term_is_caught(monkeypatch):
 def test_planted_transposed_score_operand_is_caught(monkeypatch):
     real = A._scores
 
-    def wrong(qh, kh, q_pos, k_pos, causal, scale):
-        s = real(qh, kh, q_pos, k_pos, causal, scale)
+    def wrong(qh, kh, q_pos, k_pos, causal, scale, bvis=None):
+        s = real(qh, kh, q_pos, k_pos, causal, scale, bvis)
         return s[:, ::-1].copy()  # keys in the wrong order
     monkeypatch.setattr(A, "_scores", wrong)
     assert _fails(test_fwd_matches_scalar_brute_force, BRUTE_CASES[0])
@@ -463,3 +463,122 @@ def test_planted_wrong_merge_weight_is_caught(monkeypatch):
         return o, lse - 0.0 + (np.isfinite(lse) * 1e-3)
     monkeypatch.setattr(A, "lse_merge", wrong)
     assert _fails(test_chunk_partials_merged_equal_unchunked, True)
+
+
+# --------------------------------------------------------------------------
+# block masks (block-sparse attention)
+# --------------------------------------------------------------------------
+
+def brute_fwd_allowed(q, k, v, allowed, scale):
+    """Scalar brute force over an explicit predicate allowed(i, j)."""
+    b_, hq, lq, d = q.shape
+    hkv, lk, dv = k.shape[1], k.shape[2], v.shape[3]
+    grp = hq // hkv
+    out = np.zeros((b_, hq, lq, dv))
+    lse = np.full((b_, hq, lq), -math.inf)
+    for b in range(b_):
+        for h in range(hq):
+            g = h // grp
+            for i in range(lq):
+                keys = [j for j in range(lk) if allowed(i, j)]
+                if not keys:
+                    continue
+                s = [scale * math.fsum(float(q[b, h, i, c]) * float(k[b, g, j, c])
+                                       for c in range(d)) for j in keys]
+                m = max(s)
+                e = [math.exp(x - m) for x in s]
+                tot = math.fsum(e)
+                for c in range(dv):
+                    out[b, h, i, c] = math.fsum(
+                        e[t] * float(v[b, g, j, c]) for t, j in enumerate(keys)) / tot
+                lse[b, h, i] = m + math.log(tot)
+    return out, lse
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_block_mask_matches_scalar_brute_force(causal):
+    lq, lk, blk, d = 9, 11, 2, 3
+    q, k, v = rnd((2, 4, lq, d), 201), rnd((2, 2, lk, d), 202), rnd((2, 2, lk, d + 1), 203)
+    mask = (np.random.default_rng(204).random((5, 6)) < 0.5).astype(np.uint8)
+    mask[1, :] = 0  # queries 2, 3 see nothing
+    sc = 0.8
+
+    def allowed(i, j):
+        return bool(mask[i // blk, j // blk]) and ((not causal) or j <= i)
+
+    o, lse = A.attn_fwd(q, k, v, 0, 0, causal, sc, block_mask=mask, mask_block=blk)
+    ob, lb = brute_fwd_allowed(q, k, v, allowed, sc)
+    assert np.array_equal(np.isfinite(lse), np.isfinite(lb))
+    assert np.all(o[:, :, 2:4] == 0) and np.all(lse[:, :, 2:4] == -np.inf)
+    fin = np.isfinite(lb)
+    np.testing.assert_allclose(lse[fin], lb[fin], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(o, ob, rtol=1e-13, atol=1e-13)
+
+
+def test_full_and_block_causal_masks_reduce_to_the_plain_cases():
+    n, blk = 40, 8
+    q, k, v = rnd((1, 2, n, 4), 211), rnd((1, 2, n, 4), 212), rnd((1, 2, n, 4), 213)
+    nb = n // blk
+    full = np.ones((nb, nb), np.uint8)
+    for causal in (False, True):
+        a = A.attn_fwd(q, k, v, 0, 0, causal, None)
+        b = A.attn_fwd(q, k, v, 0, 0, causal, None, block_mask=full, mask_block=blk)
+        np.testing.assert_array_equal(a[0], b[0])
+        np.testing.assert_array_equal(a[1], b[1])
+    # blocks on and below the diagonal, plus the causal rule inside them
+    tril = np.tril(np.ones((nb, nb), np.uint8))
+    a = A.attn_fwd(q, k, v, 0, 0, True, None)
+    b = A.attn_fwd(q, k, v, 0, 0, True, None, block_mask=tril, mask_block=blk)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_block_mask_backward_directional_derivative():
+    lq = lk = 24
+    blk = 4
+    q, k, v = rnd((1, 2, lq, 5), 221), rnd((1, 1, lk, 5), 222), rnd((1, 1, lk, 5), 223)
+    d_o = rnd((1, 2, lq, 5), 224)
+    mask = (np.random.default_rng(225).random((6, 6)) < 0.6).astype(np.uint8)
+    mask[:, 0] = 1
+    kw = dict(block_mask=mask, mask_block=blk)
+
+    def loss(q_, k_, v_):
+        return float((A.attn_fwd(q_, k_, v_, 0, 0, True, 0.6, **kw)[0] * d_o).sum())
+
+    grads = A.attn_bwd(q, k, v, d_o, 0, 0, True, 0.6, **kw)
+    h = 1e-6
+    for which in range(3):
+        u = rnd((q, k, v)[which].shape, 230 + which)
+        xs = [q.copy(), k.copy(), v.copy()]
+        xm = [x.copy() for x in xs]
+        xs[which] += h * u
+        xm[which] -= h * u
+        num = (loss(*xs) - loss(*xm)) / (2 * h)
+        ana = float((grads[which] * u).sum())
+        assert abs(num - ana) <= 1e-6 * max(1.0, abs(ana))
+
+
+def test_planted_transposed_block_mask_is_caught(monkeypatch):
+    real = A.block_visible
+
+    def wrong(q_idx, k_idx, block_mask, block=128):
+        return real(q_idx, k_idx, np.asarray(block_mask).T.copy()
+                    if np.asarray(block_mask).shape[0] == np.asarray(block_mask).shape[1]
+                    else block_mask, block)
+
+    monkeypatch.setattr(A, "block_visible", wrong)
+
+    def square_case():
+        lq = lk = 9
+        blk = 2
+        q, k, v = rnd((1, 2, lq, 3), 241), rnd((1, 2, lk, 3), 242), rnd((1, 2, lk, 3), 243)
+        mask = (np.random.default_rng(244).random((5, 5)) < 0.5).astype(np.uint8)
+
+        def allowed(i, j):
+            return bool(mask[i // blk, j // blk])
+        o, _ = A.attn_fwd(q, k, v, 0, 0, False, 0.8, block_mask=mask, mask_block=blk)
+        ob, _ = brute_fwd_allowed(q, k, v, allowed, 0.8)
+        np.testing.assert_allclose(o, ob, rtol=1e-13, atol=1e-13)
+
+    with pytest.raises(AssertionError):
+        square_case()
