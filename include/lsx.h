@@ -173,6 +173,37 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
                    size_t workspace_bytes, lsx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * attn_block_sparse_fwd / attn_block_sparse_bwd -- exact attention over the
+ * whole sequence restricted to a block mask (the Fine-grained Attention I/O
+ * Complexity page, abstract: the analysis extends to sparse attention; the
+ * BriefGPT BurstAttention page's related work: FlashAttention extended to a
+ * broad class of sparsity patterns).  Tiles of masked blocks are skipped by
+ * the same persistent kernels as attn_chunked_fwd / attn_chunked_bwd.
+ *   block_mask: DEVICE pointer to uint8 [ceil(Lq/128)][ceil(Lk/128)],
+ *     row-major, shared by every batch row and head; entry (i, j) nonzero
+ *     lets query rows [128 i, 128 i + 128) see keys [128 j, 128 j + 128).
+ *   causal: the causal rule (key position <= query position, both counted
+ *     from 0) applies inside the allowed blocks as well.
+ *   A query left with no visible key gets O = 0, LSE = -inf; in the
+ *   backward its rows contribute nothing.
+ *   q, k, v, o, d_o bf16 (LSX_ERR_DTYPE otherwise); dq, dk, dv bf16 or f32.
+ *   Workspace (256-byte aligned, required): at least the matching
+ *   *_workspace_size bytes (LSX_ERR_WORKSPACE otherwise).  The forward and
+ *   backward are consistent with each other and with the chunked calls.
+ * ---------------------------------------------------------------------- */
+size_t attn_block_sparse_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
+int attn_block_sparse_fwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_tensor* v,
+                          const uint8_t* block_mask, int causal, float scale,
+                          const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                          size_t workspace_bytes, lsx_stream_t stream);
+size_t attn_block_sparse_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
+int attn_block_sparse_bwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_tensor* v,
+                          const lsx_tensor* o, const lsx_tensor* lse, const lsx_tensor* d_o,
+                          const uint8_t* block_mask, int causal, float scale,
+                          const lsx_tensor* dq, const lsx_tensor* dk, const lsx_tensor* dv,
+                          void* workspace, size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * attn_chunk_bwd_noalloc -- attn_chunk_bwd for callers that cannot allocate
  * device memory when they call it (the paper has no counterpart; this is a
  * deployment convenience of the library).  Examples: an extension running

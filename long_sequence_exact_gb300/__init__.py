@@ -7,6 +7,8 @@ call does, and raises if it has not been built.
 """
 
 from .attention import (  # noqa: F401
+    block_sparse_bwd,
+    block_sparse_fwd,
     chunk_bwd,
     chunk_fwd,
     chunked_bwd,
@@ -25,7 +27,8 @@ from .attention import (  # noqa: F401
 from .autograd import ChunkedAttention, chunked_attention  # noqa: F401
 
 __all__ = [
-    "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "merge", "tree_merge",
+    "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "block_sparse_fwd",
+    "block_sparse_bwd", "merge", "tree_merge",
     "decode", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
     "set_wait_limit_ns", "status_string", "sync_status", "version", "chunked_attention",
     "ChunkedAttention",

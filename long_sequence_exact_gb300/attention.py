@@ -155,6 +155,52 @@ def chunked_bwd(q, k, v, o, lse, d_o, chunk_len, causal=True, scale=None,
     return dq, dk, dv
 
 
+def _block_mask(mask, q, k):
+    """uint8 [ceil(Lq/128), ceil(Lk/128)] contiguous on q's device."""
+    nq, nk = -(-q.shape[2] // 128), -(-k.shape[2] // 128)
+    if tuple(mask.shape) != (nq, nk):
+        raise ValueError(f"block mask must be [{nq}, {nk}] (128 x 128 blocks)")
+    return mask.to(device=q.device, dtype=torch.uint8).contiguous()
+
+
+def block_sparse_fwd(q, k, v, block_mask, causal=False, scale=None, out=None, lse=None,
+                     workspace=None):
+    """Whole-sequence forward restricted to a 128 x 128 block mask."""
+    lib = load()
+    b, h, n, d = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    m = _block_mask(block_mask, q, k)
+    vq, vk, vv, vo, vl = view(q), view(k), view(v), view(out), view(lse)
+    need = lib.attn_block_sparse_fwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk))
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    check(lib.attn_block_sparse_fwd(ctypes.byref(vq), ctypes.byref(vk), ctypes.byref(vv),
+                                    m.data_ptr(), int(bool(causal)), _scale(scale),
+                                    ctypes.byref(vo), ctypes.byref(vl), ws.data_ptr(), ws.numel(),
+                                    stream_handle()), "attn_block_sparse_fwd")
+    return out, lse
+
+
+def block_sparse_bwd(q, k, v, o, lse, d_o, block_mask, causal=False, scale=None,
+                     dq=None, dk=None, dv=None, workspace=None):
+    """Whole-sequence backward restricted to a 128 x 128 block mask."""
+    lib = load()
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    m = _block_mask(block_mask, q, k)
+    vs = [view(t) for t in (q, k, v, o, lse, d_o, dq, dk, dv)]
+    need = lib.attn_block_sparse_bwd_workspace_size(ctypes.byref(vs[0]), ctypes.byref(vs[1]))
+    ws = workspace if workspace is not None else _ws(need, q.device)
+    check(lib.attn_block_sparse_bwd(*(ctypes.byref(x) for x in vs[:6]), m.data_ptr(),
+                                    int(bool(causal)), _scale(scale),
+                                    *(ctypes.byref(x) for x in vs[6:]), ws.data_ptr(),
+                                    ws.numel(), stream_handle()), "attn_block_sparse_bwd")
+    return dq, dk, dv
+
+
 def decode_workspace_size(q, kc, chunk_len) -> int:
     lib = load()
     vq, vk = view(q), view(kc)

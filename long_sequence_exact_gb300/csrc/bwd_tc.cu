@@ -71,6 +71,11 @@ struct BwdParams {
   int64_t n_items;
   int* status;
   uint64_t wait_ns;
+  // block-sparse lists (NULL: dense tile ranges up to the causal limit)
+  const int32_t* row_count;
+  const int32_t* row_list;  // stride n_ktiles
+  const int32_t* col_count;
+  const int32_t* col_list;  // stride n_qtiles
 };
 
 // TMEM column (relative to the 128-column fp32 tile) of the packed bf16
@@ -223,6 +228,7 @@ struct DkdvSmem {
 
 struct DkdvItem {
   int64_t b, hk, j, i0, n_i, group;
+  int64_t len;  // query tiles per head of the group
 };
 
 __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
@@ -234,8 +240,17 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
   x.hk = bh % p.Hkv;
   x.group = p.Hq / p.Hkv;
   x.i0 = q_tile_begin(p, x.j);
-  x.n_i = (p.n_qtiles - x.i0) * x.group;  // (head, query tile) steps
+  x.len = p.col_list == nullptr ? p.n_qtiles - x.i0 : p.col_count[x.j];
+  x.n_i = x.len * x.group;  // (head, query tile) steps
   return x;
+}
+
+// Query head and query tile of step s of a dK/dV item.
+__device__ __forceinline__ void dkdv_step(const BwdParams& p, const DkdvItem& x, int64_t s,
+                                          int64_t& h, int64_t& i) {
+  h = x.hk * x.group + s / x.len;
+  const int64_t r = s % x.len;
+  i = p.col_list == nullptr ? x.i0 + r : p.col_list[x.j * p.n_qtiles + r];
 }
 
 // Loads one 128-row tile as D/64 boxes of [128 rows][64 cols] (row-major
@@ -356,8 +371,8 @@ __global__ void __launch_bounds__(640, 1)
         }
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
-          const int64_t h = x.hk * x.group + s / (p.n_qtiles - x.i0);
-          const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
+          int64_t h, i;
+          dkdv_step(p, x, s, h, i);
           // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV)
           if (!mbar_wait(&sm.st_empty[qs], qph ^ 1, guard)) { ok = false; break; }
           if (lane == 0) {
@@ -473,7 +488,8 @@ __global__ void __launch_bounds__(640, 1)
       const int64_t key_abs = p.kv_off + x.j * 128 + row;
       bool ok = true;
       for (int64_t s = 0; s < x.n_i; ++s) {
-        const int64_t i = x.i0 + s % (p.n_qtiles - x.i0);
+        int64_t h_unused, i;
+        dkdv_step(p, x, s, h_unused, i);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
@@ -613,8 +629,14 @@ __device__ __forceinline__ DqItem dq_item(const BwdParams& p, int64_t it) {
   x.b = bh / p.Hq;
   x.h = bh % p.Hq;
   x.hk = x.h / (p.Hq / p.Hkv);
-  x.nkv = fwd_kv_tiles(x.i, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal);
+  x.nkv = p.row_list == nullptr ? fwd_kv_tiles(x.i, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal)
+                                 : p.row_count[x.i];
   return x;
+}
+
+// Key tile at position j of a dQ item.
+__device__ __forceinline__ int64_t dq_key_tile(const BwdParams& p, const DqItem& x, int64_t j) {
+  return p.row_list == nullptr ? j : p.row_list[x.i * p.n_ktiles + j];
 }
 
 template <int D, bool kT>
@@ -681,8 +703,9 @@ __global__ void __launch_bounds__(640, 1)
         for (int64_t j = 0; j < x.nkv; ++j) {
           if (!mbar_wait(&sm.kv_empty[stage], phase ^ 1, guard)) { ok = false; break; }
           mbar_arrive_expect_tx(&sm.kv_full[stage], 2 * kTile);
-          load_tile<D, false>(sm.k[stage], &tm_k, &sm.kv_full[stage], j * 128, x.hk, x.b);
-          load_tile<D, false>(sm.v[stage], &tm_v, &sm.kv_full[stage], j * 128, x.hk, x.b);
+          const int64_t kt = dq_key_tile(p, x, j);
+          load_tile<D, false>(sm.k[stage], &tm_k, &sm.kv_full[stage], kt * 128, x.hk, x.b);
+          load_tile<D, false>(sm.v[stage], &tm_v, &sm.kv_full[stage], kt * 128, x.hk, x.b);
           if (++stage == kStages) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -700,7 +723,8 @@ __global__ void __launch_bounds__(640, 1)
           if (!mbar_wait(&sm.kt_empty, kt_phase ^ 1, guard)) { ok = false; break; }
           kt_phase ^= 1;
           mbar_arrive_expect_tx(&sm.kt_full, kTile);
-          load_tile<D, true>(sm.kt, &tm_kt, &sm.kt_full, j * 128, x.hk, x.b);
+          load_tile<D, true>(sm.kt, &tm_kt, &sm.kt_full, dq_key_tile(p, x, j) * 128, x.hk,
+                             x.b);
         }
         if (!ok) break;
       }
@@ -815,7 +839,7 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_before();
         mbar_arrive(&sm.s_free);  // S/dP columns may be overwritten now
         // visible key columns of this quarter: c <= climit
-        const int64_t kb = j * 128 + 32 * qtr;
+        const int64_t kb = dq_key_tile(p, x, j) * 128 + 32 * qtr;
         int64_t lim = 31;
         if (kb + 32 > p.Lk) lim = p.Lk - kb - 1;
         if (p.causal) {
@@ -889,7 +913,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                     const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
                     float scale, const lsx_tensor& dq, const lsx_tensor& dk,
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
-                    cudaStream_t s) {
+                    cudaStream_t s, const BlockLists* bl) {
   const bool tr = cp.kt != nullptr;
   const bool rs = cp.stats.rows != nullptr;
   CUtensorMap tq, tk, tv, tdo, tkt, trs, tones;
@@ -926,6 +950,10 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.n_qtiles = ceil_div(q.N, 128);
   p.n_ktiles = ceil_div(k.N, 128);
   p.status = ctx.status; p.wait_ns = ctx.wait_ns;
+  p.row_count = bl ? bl->row_count : nullptr;
+  p.row_list = bl ? bl->row_list : nullptr;
+  p.col_count = bl ? bl->col_count : nullptr;
+  p.col_list = bl ? bl->col_list : nullptr;
 
   // dK, dV: items (key tile, b, kv head)
   p.n_items = p.n_ktiles * q.B * k.H;
@@ -983,13 +1011,13 @@ int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                   const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
                   float scale, const lsx_tensor& dq, const lsx_tensor& dk,
                   const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
-                  cudaStream_t s) {
+                  cudaStream_t s, const BlockLists* bl) {
   if (q.D == 128)
     return launch_bwd_tc_d<128>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
-                                dk, dv, accumulate, ctx, s);
+                                dk, dv, accumulate, ctx, s, bl);
   if (q.D == 64)
     return launch_bwd_tc_d<64>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
-                               dk, dv, accumulate, ctx, s);
+                               dk, dv, accumulate, ctx, s, bl);
   return LSX_ERR_UNSUPPORTED;
 }
 

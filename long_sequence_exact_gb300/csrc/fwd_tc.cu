@@ -89,6 +89,11 @@ struct FwdParams {
   int64_t l_sb, l_sh, l_sn;
   int* status;
   uint64_t wait_ns;
+  // block-sparse lists (NULL: every key tile up to the causal limit)
+  const int32_t* pair_count;
+  const int32_t* pair_list;
+  const uint8_t* bmask;  // [n_qtiles][n_kb]
+  int64_t n_qtiles, n_kb;
 };
 
 struct Item {
@@ -105,8 +110,16 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
   x.h = bh % p.Hq;
   x.hk = x.h / (p.Hq / p.Hkv);
   for (int t = 0; t < 2; ++t)
-    x.nkv[t] = fwd_kv_tiles(2 * x.pair + t, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal);
+    x.nkv[t] = p.pair_list == nullptr
+                   ? fwd_kv_tiles(2 * x.pair + t, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal)
+                   : (2 * x.pair + t < p.n_qtiles ? p.pair_count[x.pair] : 0);
   return x;
+}
+
+// Key tile visited at position j of an item (the j-th listed tile when the
+// attention is block-sparse).
+__device__ __forceinline__ int64_t key_tile(const FwdParams& p, const Item& x, int64_t j) {
+  return p.pair_list == nullptr ? j : p.pair_list[x.pair * p.n_kb + j];
 }
 
 // Wait that ignores the abort flag but keeps the time bound (used at exit).
@@ -187,11 +200,12 @@ __global__ void __launch_bounds__(384, 1)
                       static_cast<int>(x.h), static_cast<int>(x.b));
       bool ok = true;
       for (int64_t j = 0; j < nkv; ++j) {
+        const int64_t kt = key_tile(p, x, j);
         if (!mbar_wait(&sm.k_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.k_full[stage], Cfg::kTileBytes);
         for (int sub = 0; sub < Cfg::kSub; ++sub)
           tma_load_4d(&sm.k[stage][sub * 128 * 64], &tm_k, &sm.k_full[stage],
-                      sub * 64, static_cast<int>(j * 128),
+                      sub * 64, static_cast<int>(kt * 128),
                       static_cast<int>(x.hk), static_cast<int>(x.b));
         if (!mbar_wait(&sm.v_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.v_full[stage], Cfg::kTileBytes);
@@ -199,12 +213,12 @@ __global__ void __launch_bounds__(384, 1)
           // V^T tile: D rows (d) x 128 keys, as two 64-key boxes
           for (int sub = 0; sub < 2; ++sub)
             tma_load_4d(&sm.v[stage][sub * D * 64], &tm_v, &sm.v_full[stage],
-                        static_cast<int>(j * 128 + sub * 64), 0,
+                        static_cast<int>(kt * 128 + sub * 64), 0,
                         static_cast<int>(x.hk), static_cast<int>(x.b));
         } else {
           for (int sub = 0; sub < Cfg::kSub; ++sub)
             tma_load_4d(&sm.v[stage][sub * 128 * 64], &tm_v, &sm.v_full[stage],
-                        sub * 64, static_cast<int>(j * 128),
+                        sub * 64, static_cast<int>(kt * 128),
                         static_cast<int>(x.hk), static_cast<int>(x.b));
         }
         if (++stage == kStages) { stage = 0; phase ^= 1; }
@@ -350,12 +364,15 @@ __global__ void __launch_bounds__(384, 1)
             s[96 + i] = __uint_as_float(u3[i]);
           }
         }
-        const int64_t kb = j * 128;
+        const int64_t kb = key_tile(p, x, j) * 128;
+        // a listed tile whose block this query tile does not have: all masked
+        const bool blk_off =
+            p.bmask != nullptr && p.bmask[(2 * x.pair + t) * p.n_kb + kb / 128] == 0;
         const bool need_mask =
-            (kb + 128 > p.Lk) || (p.causal && p.kv_off + kb + 127 > p.q_off + qr0);
+            blk_off || (kb + 128 > p.Lk) || (p.causal && p.kv_off + kb + 127 > p.q_off + qr0);
         if (need_mask) {
-          int64_t lim = 127;
-          if (kb + 128 > p.Lk) lim = p.Lk - kb - 1;
+          int64_t lim = blk_off ? -1 : 127;
+          if (kb + 128 > p.Lk && p.Lk - kb - 1 < lim) lim = p.Lk - kb - 1;
           if (p.causal) {
             const int64_t c2 = p.q_off + qr0 + row - p.kv_off - kb;
             if (c2 < lim) lim = c2;
@@ -519,7 +536,7 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
                     const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                     int causal, float scale, const lsx_tensor& o,
                     const lsx_tensor& lse, int accumulate, void* vt,
-                    const DeviceCtx& ctx, cudaStream_t s) {
+                    const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl) {
   CUtensorMap tq, tk, tv;
   if (!make_map_bf16_4d(&tq, q.data, q.B, q.H, q.N, q.D, q.stride_b, q.stride_h,
                         q.stride_n, 128) ||
@@ -549,6 +566,11 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
   p.lse = static_cast<float*>(lse.data);
   p.l_sb = lse.stride_b; p.l_sh = lse.stride_h; p.l_sn = lse.stride_n;
   p.status = ctx.status; p.wait_ns = ctx.wait_ns;
+  p.n_qtiles = ceil_div(q.N, 128);
+  p.pair_count = bl ? bl->pair_count : nullptr;
+  p.pair_list = bl ? bl->pair_list : nullptr;
+  p.bmask = bl ? bl->mask : nullptr;
+  p.n_kb = bl ? bl->n_kb : 0;
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   auto kern = vt != nullptr ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -569,13 +591,13 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
                   const lsx_tensor& lse, int accumulate, void* vt,
-                  const DeviceCtx& ctx, cudaStream_t s) {
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl) {
   if (q.D == 128)
     return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                                accumulate, vt, ctx, s);
+                                accumulate, vt, ctx, s, bl);
   if (q.D == 64)
     return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                               accumulate, vt, ctx, s);
+                               accumulate, vt, ctx, s, bl);
   return LSX_ERR_UNSUPPORTED;
 }
 

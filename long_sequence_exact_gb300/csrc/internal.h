@@ -23,7 +23,7 @@ int device_ctx(DeviceCtx* ctx);
 // recorded on the launching stream around every launch of kernel `kid`.
 enum KernelId {
   kKidFwdTc = 0, kKidDkdv, kKidDq, kKidRowDot, kKidMerge, kKidTreeMerge,
-  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidTranspose, kKidCount
+  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidTranspose, kKidBlockLists, kKidCount
 };
 
 // Sequence-contiguous copies (layout.cu): a bf16 [B, H, N, D] view is
@@ -91,15 +91,37 @@ int launch_simt_bwd(const lsx_tensor& q, const lsx_tensor& k,
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
                     cudaStream_t s);
 
+// Block-sparse work lists (block_sparse.cu), int32 in device memory, built
+// from a block mask [n_qb][n_kb] (uint8, 128 x 128 blocks, nonzero = visible)
+// ANDed with the causal rule (positions counted from 0 on both sides):
+//   pair: for query-tile pair p (tiles 2p, 2p+1), the key tiles visible to
+//         either tile, ascending (stride n_kb);
+//   row:  for query tile i, its visible key tiles (stride n_kb);
+//   col:  for key tile j, the query tiles that see it (stride n_qb).
+struct BlockLists {
+  const uint8_t* mask = nullptr;
+  int64_t n_qb = 0, n_kb = 0;
+  const int32_t* pair_count = nullptr;
+  const int32_t* pair_list = nullptr;
+  const int32_t* row_count = nullptr;
+  const int32_t* row_list = nullptr;
+  const int32_t* col_count = nullptr;
+  const int32_t* col_list = nullptr;
+};
+size_t block_lists_bytes(int64_t lq, int64_t lk);
+int build_block_lists(const uint8_t* mask, int64_t lq, int64_t lk, int causal, void* ws,
+                      BlockLists* out, const DeviceCtx& ctx, cudaStream_t s);
+
 // tcgen05 tensor-core forward (bf16 inputs).  vt: NULL (V read as stored,
 // d-contiguous) or fwd_tc_workspace_bytes(v) of scratch that receives a
 // key-contiguous copy of V first, which the P.V product reads faster.
 size_t fwd_tc_workspace_bytes(const lsx_tensor& v);
+// With bl non-NULL, each item visits only the key tiles of its block lists.
 int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
                   const lsx_tensor& lse, int accumulate, void* vt,
-                  const DeviceCtx& ctx, cudaStream_t s);
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
 // tcgen05 tensor-core backward (bf16 inputs).  With copies.kt non-NULL, a
 // key-contiguous copy of K is written there first and the dQ product reads
@@ -120,7 +142,7 @@ int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const BwdCopies& copies, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& dq,
                   const lsx_tensor& dk, const lsx_tensor& dv, int accumulate,
-                  const DeviceCtx& ctx, cudaStream_t s);
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
 // Split-KV decode partials (bf16 inputs, D = 128).
 int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,

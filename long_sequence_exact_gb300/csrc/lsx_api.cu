@@ -35,7 +35,7 @@ std::vector<DevCache> g_devs;
 // ------------------------------------------------------- kernel timing
 const char* const kKernelNames[kKidCount] = {
     "fwd_tc", "bwd_dkdv_tc", "bwd_dq_tc", "bwd_row_dot", "merge", "tree_merge",
-    "decode_partials", "simt_fwd", "simt_bwd", "fill", "transpose"};
+    "decode_partials", "simt_fwd", "simt_bwd", "fill", "transpose", "block_lists"};
 std::atomic<bool> g_timing{false};
 struct TimedLaunch {
   int kid;
@@ -414,6 +414,95 @@ int attn_chunked_bwd(const lsx_tensor* q, const lsx_tensor* k,
   if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
   return attn_chunk_bwd(q, k, v, o, lse, d_o, 0, 0, causal, scale, dq, dk, dv, 0,
                         workspace, workspace_bytes, stream);
+}
+
+// ------------------------------------------------- block-sparse attention
+// Workspace: [V^T copy (forward) | delta, K^T copy, row statistics
+// (backward)] then the block lists, each part 256-byte aligned.
+size_t attn_block_sparse_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+  if (q == nullptr || k == nullptr || q->dtype != LSX_BF16) return 0;
+  return attn_chunk_fwd_workspace_size(q, k) + block_lists_bytes(q->N, k->N);
+}
+
+size_t attn_block_sparse_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
+  if (q == nullptr || k == nullptr || q->dtype != LSX_BF16) return 0;
+  return attn_chunk_bwd_workspace_size(q, k) + block_lists_bytes(q->N, k->N);
+}
+
+int attn_block_sparse_fwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_tensor* v,
+                          const uint8_t* block_mask, int causal, float scale,
+                          const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                          size_t workspace_bytes, lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, k, v));
+  if (q->dtype != LSX_BF16) return LSX_ERR_DTYPE;
+  if (block_mask == nullptr) return LSX_ERR_NULL;
+  LSX_TRY(check_view(o));
+  if (o->B != q->B || o->H != q->H || o->N != q->N || o->D != q->D) return LSX_ERR_SHAPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_lse(lse, q));
+  if (workspace == nullptr || workspace_bytes < attn_block_sparse_fwd_workspace_size(q, k))
+    return LSX_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const float sc = resolve_scale(scale, q->D);
+  cudaStream_t s = as_stream(stream);
+  if (q->N == 0) return LSX_OK;
+  if (k->N == 0) return launch_fill_empty(*o, *lse, ctx, s);
+  void* vt = workspace;
+  void* lists = static_cast<char*>(workspace) + attn_chunk_fwd_workspace_size(q, k);
+  BlockLists bl;
+  LSX_TRY(build_block_lists(block_mask, q->N, k->N, causal != 0, lists, &bl, ctx, s));
+  return launch_fwd_tc(*q, *k, *v, 0, 0, causal != 0, sc, *o, *lse, 0, vt, ctx, s, &bl);
+}
+
+int attn_block_sparse_bwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_tensor* v,
+                          const lsx_tensor* o, const lsx_tensor* lse, const lsx_tensor* d_o,
+                          const uint8_t* block_mask, int causal, float scale,
+                          const lsx_tensor* dq, const lsx_tensor* dk, const lsx_tensor* dv,
+                          void* workspace, size_t workspace_bytes, lsx_stream_t stream) {
+  LSX_TRY(check_qkv(q, k, v));
+  if (q->dtype != LSX_BF16) return LSX_ERR_DTYPE;
+  if (block_mask == nullptr) return LSX_ERR_NULL;
+  LSX_TRY(check_view(o));
+  LSX_TRY(check_view(d_o));
+  LSX_TRY(check_view(dq));
+  LSX_TRY(check_view(dk));
+  LSX_TRY(check_view(dv));
+  if (!same_bhn_d(o, q) || !same_bhn_d(d_o, q) || !same_bhn_d(dq, q) ||
+      !same_bhn_d(dk, k) || !same_bhn_d(dv, k))
+    return LSX_ERR_SHAPE;
+  if (d_o->dtype != q->dtype) return LSX_ERR_DTYPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_row_aligned(d_o));
+  LSX_TRY(check_row_aligned(dq));
+  LSX_TRY(check_row_aligned(dk));
+  LSX_TRY(check_row_aligned(dv));
+  LSX_TRY(check_lse(lse, q));
+  if (workspace == nullptr || workspace_bytes < attn_block_sparse_bwd_workspace_size(q, k))
+    return LSX_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const float sc = resolve_scale(scale, q->D);
+  cudaStream_t s = as_stream(stream);
+  if (q->N == 0 || k->N == 0) {
+    if (q->N > 0) LSX_TRY(launch_zero(*dq, ctx, s));
+    if (k->N > 0) {
+      LSX_TRY(launch_zero(*dk, ctx, s));
+      LSX_TRY(launch_zero(*dv, ctx, s));
+    }
+    return LSX_OK;
+  }
+  const size_t need = attn_chunk_bwd_min_workspace_size(q, k);
+  const BwdCopies copies = bwd_tc_copies(*q, *k, static_cast<char*>(workspace) + need);
+  void* lists = static_cast<char*>(workspace) + attn_chunk_bwd_workspace_size(q, k);
+  BlockLists bl;
+  LSX_TRY(build_block_lists(block_mask, q->N, k->N, causal != 0, lists, &bl, ctx, s));
+  float* delta = static_cast<float*>(workspace);
+  LSX_TRY(launch_row_dot(*o, *d_o, delta, copies.stats, lse, sc, ctx, s));
+  return launch_bwd_tc(*q, *k, *v, *lse, *d_o, delta, copies, 0, 0, causal != 0, sc, *dq,
+                       *dk, *dv, 0, ctx, s, &bl);
 }
 
 // ----------------------------------------------------------- attn_decode
