@@ -317,6 +317,9 @@ def secondary(dev, pk):
       causal_32k_ring, noncausal_64k_heavytail
                   chunked fwd+bwd of the other two attention workloads
                   (TFLOP/s against the sustained bf16 peak)
+      block_sparse_window_128k
+                  block-sparse fwd+bwd at 128K with a sliding-window block
+                  mask (only visible pairs credited)
       autograd_remat_32k
                   backward time through torch.autograd with the checkpoint
                   at the attention output vs at the layer input (re-run)
@@ -402,6 +405,36 @@ def secondary(dev, pk):
         del x, q, k, v, d_o, o, lse, grads
         torch.cuda.empty_cache()
     out["tflops_peak"] = pk["bf16_sustained"]
+    # block-sparse: causal sliding window of 32 blocks (4096 keys) at 128K
+    w = WORKLOADS["causal_128k_balanced"]
+    x = make_inputs(w, device=dev)
+    q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
+    nb = w.N // 128
+    win = 32
+    mask = torch.zeros((nb, nb), dtype=torch.uint8)
+    for i in range(nb):
+        mask[i, max(0, i - win + 1):i + 1] = 1
+    mask = mask.to(dev)
+    o, lse = lsx.block_sparse_fwd(q, k, v, mask, True)
+    grads = lsx.block_sparse_bwd(q, k, v, o, lse, d_o, mask, True)
+
+    def bs_step():
+        lsx.block_sparse_fwd(q, k, v, mask, True, out=o, lse=lse)
+        lsx.block_sparse_bwd(q, k, v, o, lse, d_o, mask, True, dq=grads[0], dk=grads[1],
+                             dv=grads[2])
+
+    ms = timed(bs_step)
+    # visible pairs: full off-diagonal blocks plus causal diagonal blocks
+    blocks = int(mask.sum().item())
+    pairs = (blocks - nb) * 128 * 128 + nb * 128 * 129 // 2
+    fl = 4.0 * w.B * w.Hq * pairs * w.D * 3.5
+    tf = fl / (ms / 1e3) / 1e12
+    out["block_sparse_window_128k"] = {
+        "tflops": round(tf, 1), "frac": round(tf / pk["bf16_sustained"], 4), "ms": round(ms, 3),
+        "flops": fl, "blocks_computed": blocks, "blocks_causal": nb * (nb + 1) // 2,
+        "workload": "causal_128k_balanced with a 32-block (4096-key) sliding-window block mask"}
+    del x, q, k, v, d_o, o, lse, grads, mask
+    torch.cuda.empty_cache()
     # backward through torch.autograd with the checkpoint at the attention
     # output (O, LSE kept) against the layer-boundary form (forward re-run)
     w = WORKLOADS["causal_32k_ring"]
