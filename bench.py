@@ -46,6 +46,19 @@ DRAM_BYTES_128K = {"fwd_tc": 28.17e9 + 1.38e9, "bwd_dkdv_tc": 42.16e9 + 2.15e9,
                    "bwd_dq_tc": 39.92e9 + 1.07e9}
 
 
+def job_throughput(ms_local, work_per_step, steps, world, device="cpu"):
+    """Whole-job rate over N ranks that each did `steps` steps of
+    `work_per_step` units in `ms_local` ms: the slowest rank's time (a MAX
+    all-reduce when world > 1) sets it.  Returns (ms_max, units per second / 1e12)."""
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world * work_per_step * steps / (ms_max / 1e3) / 1e12
+
+
 def flops(b, h, n, d, causal=True):
     pairs = n * (n + 1) / 2 if causal else n * n
     fwd = 4.0 * b * h * pairs * d
@@ -196,14 +209,9 @@ def run_ours(args, rank, world, local_rank):
     if lsx.sync_status() != 0:
         raise RuntimeError("device status after the timed steps")
 
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-
     f_fwd, f_bwd = flops(w.B, w.Hq, w.N, w.D)
     step_flops = f_fwd + f_bwd
-    value = world * step_flops * args.steps / (ms_max / 1e3) / 1e12
+    ms_max, value = job_throughput(ms, step_flops, args.steps, world, dev)
 
     # end to end through the same C ABI, inputs copied in from pinned host
     # memory and every output copied back, each step
@@ -237,10 +245,8 @@ def run_ours(args, rank, world, local_rank):
             e2e_step()
         b_.record(stream)
         torch.cuda.synchronize()
-        te = torch.tensor([a.elapsed_time(b_)], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        e2e = {"value": round(world * step_flops * n_e2e / (float(te.item()) / 1e3) / 1e12, 2),
+        _, e2e_value = job_throughput(a.elapsed_time(b_), step_flops, n_e2e, world, dev)
+        e2e = {"value": round(e2e_value, 2),
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e2e}
 
