@@ -281,6 +281,27 @@ int attn_decode(const lsx_tensor* q, const lsx_tensor* kc,
                 size_t workspace_bytes, lsx_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * attn_decode_tree -- one decode step for B branches of a tree of sequences
+ * that share a prefix (Tree Attention page, related work: DeFT, tree-
+ * structured decoding with KV-guided grouping): branch b's query attends to
+ * the shared prefix followed by its own suffix.  The prefix cache is read
+ * once per group of branches (up to 64 / G branches, G = Hq / Hkv), not once
+ * per branch; the suffixes are read once each; all partials are merged in
+ * one tree reduction.
+ *   q [B, Hq, 1, D] bf16; pk, pv [1, Hkv, Np, D] bf16 (the shared prefix);
+ *   sk, sv [B, Hkv, Ns, D] bf16 (the suffixes, Ns may be 0; NULL tensors
+ *   are allowed when Ns == 0); o [B, Hq, 1, D] bf16 or f32; lse [B, Hq, 1, 1]
+ *   f32.  Hq / Hkv in {1, 2, 4, 8}, D == 128, chunk_len a multiple of 128.
+ * Workspace: attn_decode_tree_workspace_size bytes (the partials of both).
+ * ---------------------------------------------------------------------- */
+size_t attn_decode_tree_workspace_size(const lsx_tensor* q, const lsx_tensor* pk,
+                                       const lsx_tensor* sk, int64_t chunk_len);
+int attn_decode_tree(const lsx_tensor* q, const lsx_tensor* pk, const lsx_tensor* pv,
+                     const lsx_tensor* sk, const lsx_tensor* sv, int64_t chunk_len,
+                     float scale, const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                     size_t workspace_bytes, lsx_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Status, diagnostics and host-side helpers.
  * ---------------------------------------------------------------------- */
 

@@ -14,6 +14,7 @@ from .attention import (  # noqa: F401
     chunked_bwd,
     chunked_fwd,
     decode,
+    decode_tree,
     decode_workspace_size,
     merge,
     schedule_stats,
@@ -29,7 +30,7 @@ from .autograd import ChunkedAttention, chunked_attention  # noqa: F401
 __all__ = [
     "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "block_sparse_fwd",
     "block_sparse_bwd", "merge", "tree_merge",
-    "decode", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
+    "decode", "decode_tree", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
     "set_wait_limit_ns", "status_string", "sync_status", "version", "chunked_attention",
     "ChunkedAttention",
 ]

@@ -57,6 +57,8 @@ SIGNATURES = {
     "attn_merge": (_INT, [_P, _P, _P, _P, _P, _P, _VP]),
     "attn_tree_merge": (_INT, [_P, _I64, _P, _I64, _INT, _P, _P, _VP]),
     "attn_chunk_bwd_min_workspace_size": (_SZ, [_P, _P]),
+    "attn_decode_tree_workspace_size": (_SZ, [_P, _P, _P, _I64]),
+    "attn_decode_tree": (_INT, [_P, _P, _P, _P, _P, _I64, ctypes.c_float, _P, _P, _VP, _SZ, _VP]),
     "attn_block_sparse_fwd_workspace_size": (_SZ, [_P, _P]),
     "attn_block_sparse_fwd": (_INT, [_P, _P, _P, _VP, _INT, ctypes.c_float, _P, _P, _VP, _SZ, _VP]),
     "attn_block_sparse_bwd_workspace_size": (_SZ, [_P, _P]),

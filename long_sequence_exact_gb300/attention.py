@@ -227,6 +227,32 @@ def decode(q, kc, vc, chunk_len, scale=None, out=None, lse=None, workspace=None,
     return out, lse
 
 
+def decode_tree(q, pk, pv, sk, sv, chunk_len, scale=None, out=None, lse=None, workspace=None,
+                out_dtype=None):
+    """One decode step of B branches sharing the prefix cache (pk, pv
+    [1, Hkv, Np, D]); sk, sv [B, Hkv, Ns, D] are the branches' own suffixes
+    (None when there are none).  The prefix is read once per branch group."""
+    lib = load()
+    b, h, n, d = q.shape
+    if out is None:
+        out = torch.empty((b, h, n, d), dtype=out_dtype or q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((b, h, n), dtype=torch.float32, device=q.device)
+    vq, vpk, vpv, vo, vl = view(q), view(pk), view(pv), view(out), view(lse)
+    vsk = view(sk) if sk is not None else None
+    vsv = view(sv) if sv is not None else None
+    rs = (lambda t: ctypes.byref(t) if t is not None else None)
+    need = lib.attn_decode_tree_workspace_size(ctypes.byref(vq), ctypes.byref(vpk), rs(vsk),
+                                               int(chunk_len))
+    if workspace is None:
+        workspace = _ws(need, q.device)
+    check(lib.attn_decode_tree(ctypes.byref(vq), ctypes.byref(vpk), ctypes.byref(vpv), rs(vsk),
+                               rs(vsv), int(chunk_len), _scale(scale), ctypes.byref(vo),
+                               ctypes.byref(vl), workspace.data_ptr(), workspace.numel(),
+                               stream_handle()), "attn_decode_tree")
+    return out, lse
+
+
 def sync_status(stream=None) -> int:
     """Synchronise, return and clear the device status word (0 = ok)."""
     return int(load().lsx_sync_status(stream_handle(stream)))

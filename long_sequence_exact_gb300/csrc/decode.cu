@@ -51,6 +51,9 @@ struct DecodeParams {
   float* part_l;
   int* status;
   uint64_t wait_ns;
+  int64_t G;      // query heads per kv head
+  int64_t part0;  // first partial block written (chunk c writes part0 + c)
+  int64_t qb0;    // query batch of cache batch 0 (row r of a CTA adds r / G)
 };
 
 __device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&x)[4]) {
@@ -178,17 +181,26 @@ __global__ void __launch_bounds__(256) decode_partials_kernel(DecodeParams p) {
       }
     }
     const int64_t row = b * p.Hq + hk * G + g;
-    p.part_o[(chunk * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
+    p.part_o[((p.part0 + chunk) * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
     if (d == 0)
-      p.part_l[chunk * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
+      p.part_l[(p.part0 + chunk) * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
   }
 }
 
-template <int G>
+// Rows per CTA, R = GW * RG: every query row that reads this CTA's cache
+// chunk (the G heads of a kv head, or, for a shared prefix, the G heads of
+// every branch).  Warp w takes rows [GW (w % RG), GW (w % RG) + GW) and key
+// group w / RG of KG = 8 / RG; per stage it runs kSub sub-steps of
+// KPI = 32 / GW keys, so every (row, key) pair of a stage is scored by one
+// warp and each row's partial states come from the KG warps of its group.
+template <int GW, int RG>
 struct DecodeTmaCfg {
-  static constexpr int kKpi = 32 / G;               // keys per warp per stage
-  static constexpr int kKeys = kWarps * kKpi;       // keys per stage
-  static constexpr int kStages = G == 2 ? 2 : (G == 4 ? 3 : 4);
+  static constexpr int kR = GW * RG;
+  static constexpr int kKpi = 32 / GW;
+  static constexpr int kKg = kWarps / RG;
+  static constexpr int kSub = (kKg * kKpi >= 64) ? 1 : 64 / (kKg * kKpi);
+  static constexpr int kKeys = kKg * kKpi * kSub;   // keys per stage
+  static constexpr int kStages = kKeys >= 128 ? 2 : 3;
   static constexpr int kBox = kKeys * 128;          // one [kKeys][64] bf16 box
   static constexpr int kStageBytes = 4 * kBox;      // K and V, two boxes each
   static constexpr int kSmem = kStages * kStageBytes + 256;
@@ -206,11 +218,14 @@ __device__ __forceinline__ void row4(const uint8_t* tile, int box_bytes, int r, 
   x[2] = __low2float(b); x[3] = __high2float(b);
 }
 
-template <int G>
-__global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
+// Grid (chunks, Hkv, cache batches).  Query row r of a CTA is query head
+// hk G + r % G of query batch (cache batch + r / G); its partial goes to
+// row (that batch) Hq + head of the partial block `part0 + chunk`.
+template <int GW, int RG>
+__global__ void __launch_bounds__(32 * (kWarps + 1), GW == 8 ? 1 : 2)
     decode_tma_kernel(const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
-  using C = DecodeTmaCfg<G>;
+  using C = DecodeTmaCfg<GW, RG>;
   constexpr int KPI = C::kKpi;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
@@ -218,8 +233,8 @@ __global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + C::kStages * C::kStageBytes);
   uint64_t* empty = full + C::kStages;
   int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
-  __shared__ float s_m[kWarps][G];
-  __shared__ float s_l[kWarps][G];
+  __shared__ float s_m[kWarps][GW];
+  __shared__ float s_l[kWarps][GW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
   const int64_t k0 = chunk * p.chunk_len;
@@ -236,10 +251,11 @@ __global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
   }
   __syncthreads();
 
-  float m = kNegInf, l = 0.f;  // state of head (lane % G)
-  float o[G][4];
+  const int rg = warp % RG, kg = warp / RG;
+  float m = kNegInf, l = 0.f;  // state of row GW rg + lane % GW
+  float o[GW][4];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int g = 0; g < GW; ++g)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[g][e] = 0.f;
 
@@ -263,10 +279,12 @@ __global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
     }
   } else {
     // ------------------------------------------------------- compute warps
-    float qv[G][4];
+    float qv[GW][4];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      load4(p.q + b * p.q_sb + (hk * G + g) * p.q_sh + lane * 4, qv[g]);
+    for (int g = 0; g < GW; ++g) {
+      const int r = rg * GW + g;
+      load4(p.q + (p.qb0 + b + r / p.G) * p.q_sb + (hk * p.G + r % p.G) * p.q_sh + lane * 4,
+            qv[g]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) qv[g][e] *= p.scale_log2;
     }
@@ -275,61 +293,65 @@ __global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
       if (!mbar_wait(&full[stg], static_cast<uint32_t>(s / C::kStages) & 1, guard)) break;
       const uint8_t* kt = stages + stg * C::kStageBytes;
       const uint8_t* vt = kt + 2 * C::kBox;
-      const int64_t base = k0 + s * C::kKeys + warp * KPI;
-      // partial dots, index i = kk * G + g
-      float part[32];
+      for (int u = 0; u < C::kSub; ++u) {
+        const int r0 = (u * C::kKg + kg) * KPI;  // first key of the sub-step in the stage
+        const int64_t base = k0 + s * C::kKeys + r0;
+        // partial dots, index i = kk * GW + g
+        float part[32];
 #pragma unroll
-      for (int kk = 0; kk < KPI; ++kk) {
-        float kr[4];
-        row4(kt, C::kBox, warp * KPI + kk, lane, kr);
+        for (int kk = 0; kk < KPI; ++kk) {
+          float kr[4];
+          row4(kt, C::kBox, r0 + kk, lane, kr);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float a = 0.f;
+          for (int g = 0; g < GW; ++g) {
+            float a = 0.f;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) a = fmaf(qv[g][e], kr[e], a);
-          part[kk * G + g] = a;
+            for (int e = 0; e < 4; ++e) a = fmaf(qv[g][e], kr[e], a);
+            part[kk * GW + g] = a;
+          }
         }
-      }
-      // transpose-reduce: afterwards part[0] = full sum of index `lane`
+        // transpose-reduce: afterwards part[0] = full sum of index `lane`
 #pragma unroll
-      for (int half = 16; half >= 1; half >>= 1) {
-        const bool up = (lane & half) != 0;
+        for (int half = 16; half >= 1; half >>= 1) {
+          const bool up = (lane & half) != 0;
 #pragma unroll
-        for (int i = 0; i < half; ++i) {
-          const float send = up ? part[i] : part[i + half];
-          const float keep = up ? part[i + half] : part[i];
-          part[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+          for (int i = 0; i < half; ++i) {
+            const float send = up ? part[i] : part[i + half];
+            const float keep = up ? part[i + half] : part[i];
+            part[i] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+          }
         }
-      }
-      float sc = part[0];
-      if (base + lane / G >= k1) sc = kNegInf;  // past the chunk (zero-filled rows)
-      float mx = sc;
+        float sc = part[0];
+        if (base + lane / GW >= k1) sc = kNegInf;  // past the chunk (zero-filled rows)
+        float mx = sc;
 #pragma unroll
-      for (int off = G; off < 32; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-      const float m_new = fmaxf(m, mx);
-      const float alpha = (m == kNegInf) ? 0.f : ex2(m - m_new);
-      const float mu = (m_new == kNegInf) ? 0.f : m_new;
-      const float pr = ex2(sc - mu);
-      float ps = pr;
+        for (int off = GW; off < 32; off <<= 1)
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m, mx);
+        const float alpha = (m == kNegInf) ? 0.f : ex2(m - m_new);
+        const float mu = (m_new == kNegInf) ? 0.f : m_new;
+        const float pr = ex2(sc - mu);
+        float ps = pr;
 #pragma unroll
-      for (int off = G; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
-      l = l * alpha + ps;
-      m = m_new;
+        for (int off = GW; off < 32; off <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        l = l * alpha + ps;
+        m = m_new;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float ag = __shfl_sync(0xffffffffu, alpha, g);
+        for (int g = 0; g < GW; ++g) {
+          const float ag = __shfl_sync(0xffffffffu, alpha, g);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) o[g][e] *= ag;
-      }
+          for (int e = 0; e < 4; ++e) o[g][e] *= ag;
+        }
 #pragma unroll
-      for (int kk = 0; kk < KPI; ++kk) {
-        float vr[4];
-        row4(vt, C::kBox, warp * KPI + kk, lane, vr);
+        for (int kk = 0; kk < KPI; ++kk) {
+          float vr[4];
+          row4(vt, C::kBox, r0 + kk, lane, vr);
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pkg = __shfl_sync(0xffffffffu, pr, kk * G + g);
+          for (int g = 0; g < GW; ++g) {
+            const float pkg = __shfl_sync(0xffffffffu, pr, kk * GW + g);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) o[g][e] = fmaf(pkg, vr[e], o[g][e]);
+            for (int e = 0; e < 4; ++e) o[g][e] = fmaf(pkg, vr[e], o[g][e]);
+          }
         }
       }
       __syncwarp();
@@ -339,62 +361,76 @@ __global__ void __launch_bounds__(32 * (kWarps + 1), G == 8 ? 1 : 2)
   // merge the warps' states; the per-warp O rows reuse the stage memory once
   // every stage has been consumed
   __syncthreads();
-  float* s_o = reinterpret_cast<float*>(stages);  // [kWarps][G][128]
+  float* s_o = reinterpret_cast<float*>(stages);  // [kWarps][GW][128]
   if (warp < kWarps) {
-    if (lane < G) {
+    if (lane < GW) {
       s_m[warp][lane] = m;
       s_l[warp][lane] = l;
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
+    for (int g = 0; g < GW; ++g)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s_o[(warp * G + g) * 128 + lane * 4 + e] = o[g][e];
+      for (int e = 0; e < 4; ++e) s_o[(warp * GW + g) * 128 + lane * 4 + e] = o[g][e];
   }
   __syncthreads();
-  for (int idx = threadIdx.x; idx < G * 128; idx += blockDim.x) {
-    const int g = idx / 128, d = idx % 128;
+  for (int idx = threadIdx.x; idx < C::kR * 128; idx += blockDim.x) {
+    const int r = idx / 128, d = idx % 128;
+    const int rgr = r / GW, g = r % GW;
     float mm = kNegInf;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) mm = fmaxf(mm, s_m[w][g]);
+    for (int w = rgr; w < kWarps; w += RG) mm = fmaxf(mm, s_m[w][g]);
     float tot = 0.f, acc = 0.f;
     if (mm != kNegInf) {
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
+      for (int w = rgr; w < kWarps; w += RG) {
         const float f = (s_m[w][g] == kNegInf) ? 0.f : ex2(s_m[w][g] - mm);
         tot += s_l[w][g] * f;
-        acc += s_o[(w * G + g) * 128 + d] * f;
+        acc += s_o[(w * GW + g) * 128 + d] * f;
       }
     }
-    const int64_t row = b * p.Hq + hk * G + g;
-    p.part_o[(chunk * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
+    const int64_t row = (p.qb0 + b + r / p.G) * p.Hq + hk * p.G + r % p.G;
+    const int64_t part = p.part0 + chunk;
+    p.part_o[(part * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
     if (d == 0)
-      p.part_l[chunk * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
+      p.part_l[part * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
   }
 }
 
-template <int G>
+template <int GW, int RG>
 bool launch_decode_tma(const lsx_tensor& kc, const lsx_tensor& vc, const DecodeParams& p,
                        dim3 grid, cudaStream_t s) {
-  using C = DecodeTmaCfg<G>;
+  using C = DecodeTmaCfg<GW, RG>;
   CUtensorMap tk, tv;
   if (!make_map_bf16_4d(&tk, kc.data, kc.B, kc.H, kc.N, kc.D, kc.stride_b, kc.stride_h,
                         kc.stride_n, C::kKeys, false) ||
       !make_map_bf16_4d(&tv, vc.data, vc.B, vc.H, vc.N, vc.D, vc.stride_b, vc.stride_h,
                         vc.stride_n, C::kKeys, false))
     return false;  // layout the TMA cannot describe: the register kernel runs
-  if (cudaFuncSetAttribute(decode_tma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::kSmem) != cudaSuccess)
+  if (cudaFuncSetAttribute(decode_tma_kernel<GW, RG>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess)
     return false;
-  decode_tma_kernel<G><<<grid, 32 * (kWarps + 1), C::kSmem, s>>>(tk, tv, p);
+  decode_tma_kernel<GW, RG><<<grid, 32 * (kWarps + 1), C::kSmem, s>>>(tk, tv, p);
   return true;
+}
+
+// Rows per CTA R (a multiple of 2 up to 64): picks the (GW, RG) instance.
+bool launch_decode_rows(int64_t R, const lsx_tensor& kc, const lsx_tensor& vc,
+                        const DecodeParams& p, dim3 grid, cudaStream_t s) {
+  switch (R) {
+    case 2: return launch_decode_tma<2, 1>(kc, vc, p, grid, s);
+    case 4: return launch_decode_tma<4, 1>(kc, vc, p, grid, s);
+    case 8: return launch_decode_tma<8, 1>(kc, vc, p, grid, s);
+    case 16: return launch_decode_tma<8, 2>(kc, vc, p, grid, s);
+    case 32: return launch_decode_tma<8, 4>(kc, vc, p, grid, s);
+    case 64: return launch_decode_tma<8, 8>(kc, vc, p, grid, s);
+    default: return false;
+  }
 }
 
 }  // namespace
 
-int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
-                           const lsx_tensor& vc, int64_t chunk_len,
-                           float scale, float* part_o, float* part_lse,
-                           const DeviceCtx& ctx, cudaStream_t s) {
+namespace {
+DecodeParams decode_params(const lsx_tensor& q, const lsx_tensor& kc, const lsx_tensor& vc,
+                           int64_t chunk_len, float scale, float* part_o, float* part_lse,
+                           int64_t part0, const DeviceCtx& ctx) {
   DecodeParams p;
   p.q = static_cast<const __nv_bfloat16*>(q.data);
   p.q_sb = q.stride_b; p.q_sh = q.stride_h;
@@ -407,24 +443,65 @@ int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
   p.scale_log2 = scale * kLog2e;
   p.part_o = part_o; p.part_l = part_lse;
   p.status = ctx.status; p.wait_ns = ctx.wait_ns;
+  p.G = q.H / kc.H;
+  p.part0 = part0;
+  p.qb0 = 0;
+  return p;
+}
+}  // namespace
+
+int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
+                           const lsx_tensor& vc, int64_t chunk_len,
+                           float scale, float* part_o, float* part_lse,
+                           const DeviceCtx& ctx, cudaStream_t s, int64_t part0) {
+  DecodeParams p = decode_params(q, kc, vc, chunk_len, scale, part_o, part_lse, part0, ctx);
   const int64_t parts = ceil_div(kc.N, chunk_len);
   if (parts > 65535 * 1024LL || kc.H > 65535 || q.B > 65535) return LSX_ERR_UNSUPPORTED;
   dim3 grid(static_cast<unsigned>(parts), static_cast<unsigned>(kc.H),
             static_cast<unsigned>(q.B));
   timing_begin(kKidDecode, s);
-  bool done = false;
-  switch (q.H / kc.H) {
-    case 2: done = launch_decode_tma<2>(kc, vc, p, grid, s); break;
-    case 4: done = launch_decode_tma<4>(kc, vc, p, grid, s); break;
-    case 8: done = launch_decode_tma<8>(kc, vc, p, grid, s); break;
-    default: break;
-  }
+  bool done = p.G >= 2 && launch_decode_rows(p.G, kc, vc, p, grid, s);
   if (!done) switch (q.H / kc.H) {
     case 1: decode_partials_kernel<1><<<grid, 256, 0, s>>>(p); break;
     case 2: decode_partials_kernel<2><<<grid, 256, 0, s>>>(p); break;
     case 4: decode_partials_kernel<4><<<grid, 256, 0, s>>>(p); break;
     case 8: decode_partials_kernel<8><<<grid, 256, 0, s>>>(p); break;
     default: return LSX_ERR_UNSUPPORTED;
+  }
+  timing_end(kKidDecode, s);
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+// Partials of every branch's queries against one shared cache (batch 1):
+// the branches are taken `group` at a time, each group's B_g * G query rows
+// reading the cache once (DeFT, KV-guided grouping).
+int launch_decode_shared(const lsx_tensor& q, const lsx_tensor& kc, const lsx_tensor& vc,
+                         int64_t chunk_len, float scale, float* part_o, float* part_lse,
+                         const DeviceCtx& ctx, cudaStream_t s, int64_t part0) {
+  DecodeParams p = decode_params(q, kc, vc, chunk_len, scale, part_o, part_lse, part0, ctx);
+  const int64_t parts = ceil_div(kc.N, chunk_len);
+  if (parts > 65535 * 1024LL || kc.H > 65535) return LSX_ERR_UNSUPPORTED;
+  if (q.B == 1)  // one branch: the cache's batch is the query's
+    return launch_decode_partials(q, kc, vc, chunk_len, scale, part_o, part_lse, ctx, s, part0);
+  // largest power-of-two branch group with group * G rows <= 64
+  int64_t group = 1;
+  while (group * 2 <= q.B && group * 2 * p.G <= 64) group *= 2;
+  dim3 grid(static_cast<unsigned>(parts), static_cast<unsigned>(kc.H), 1u);
+  timing_begin(kKidDecode, s);
+  for (int64_t b0 = 0; b0 < q.B;) {
+    int64_t g = group;
+    while (g > q.B - b0) g /= 2;  // the tail: the largest power of two that fits
+    int64_t start = b0;
+    if (g * p.G < 2) {  // one query row left (G = 1): redo the last two branches
+      g = 2;
+      start = q.B - 2;
+    }
+    p.qb0 = start;
+    if (!launch_decode_rows(g * p.G, kc, vc, p, grid, s)) {
+      timing_end(kKidDecode, s);
+      return LSX_ERR_UNSUPPORTED;
+    }
+    b0 = start + g;
   }
   timing_end(kKidDecode, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;

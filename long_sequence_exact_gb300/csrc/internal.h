@@ -144,11 +144,17 @@ int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& dk, const lsx_tensor& dv, int accumulate,
                   const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
-// Split-KV decode partials (bf16 inputs, D = 128).
+// Split-KV decode partials (bf16 inputs, D = 128): chunk c of the cache
+// writes partial block part0 + c, [parts][B * Hq][D] and [parts][B * Hq].
 int launch_decode_partials(const lsx_tensor& q, const lsx_tensor& kc,
                            const lsx_tensor& vc, int64_t chunk_len,
                            float scale, float* part_o, float* part_lse,
-                           const DeviceCtx& ctx, cudaStream_t s);
+                           const DeviceCtx& ctx, cudaStream_t s, int64_t part0 = 0);
+// The same against one cache (batch 1) shared by all B query batches, read
+// once per group of branches.
+int launch_decode_shared(const lsx_tensor& q, const lsx_tensor& kc, const lsx_tensor& vc,
+                         int64_t chunk_len, float scale, float* part_o, float* part_lse,
+                         const DeviceCtx& ctx, cudaStream_t s, int64_t part0);
 
 // Host-side forward work schedule shared with the forward kernel: the
 // order in which work items are handed to persistent CTAs.

@@ -556,6 +556,79 @@ int attn_decode(const lsx_tensor* q, const lsx_tensor* kc,
                            *lse, ctx, s);
 }
 
+// ------------------------------------------------------- attn_decode_tree
+namespace {
+int64_t tree_parts(const lsx_tensor* pk, const lsx_tensor* sk, int64_t chunk_len) {
+  const int64_t ns = (sk == nullptr || sk->data == nullptr) ? 0 : sk->N;
+  return ceil_div(pk->N, chunk_len) + ceil_div(ns, chunk_len);
+}
+}  // namespace
+
+size_t attn_decode_tree_workspace_size(const lsx_tensor* q, const lsx_tensor* pk,
+                                       const lsx_tensor* sk, int64_t chunk_len) {
+  if (q == nullptr || pk == nullptr || chunk_len <= 0) return 0;
+  const int64_t parts = tree_parts(pk, sk, chunk_len);
+  const int64_t rows = q->B * q->H;
+  const size_t o_bytes = static_cast<size_t>(parts * rows * q->D) * sizeof(float);
+  const size_t l_bytes = static_cast<size_t>(parts * rows) * sizeof(float);
+  return ((o_bytes + 255) / 256) * 256 + ((l_bytes + 255) / 256) * 256;
+}
+
+int attn_decode_tree(const lsx_tensor* q, const lsx_tensor* pk, const lsx_tensor* pv,
+                     const lsx_tensor* sk, const lsx_tensor* sv, int64_t chunk_len,
+                     float scale, const lsx_tensor* o, const lsx_tensor* lse, void* workspace,
+                     size_t workspace_bytes, lsx_stream_t stream) {
+  if (q == nullptr || pk == nullptr) return LSX_ERR_NULL;
+  if (pk->B != 1) return LSX_ERR_SHAPE;
+  {
+    lsx_tensor q1 = *q;  // the prefix is one cache for every branch
+    q1.B = 1;
+    LSX_TRY(check_qkv(&q1, pk, pv));
+    LSX_TRY(check_view(q));
+  }
+  if (q->dtype != LSX_BF16) return LSX_ERR_DTYPE;
+  if (q->N != 1 || q->D != 128) return LSX_ERR_SHAPE;
+  const bool has_suffix = sk != nullptr && sk->data != nullptr && sk->N > 0;
+  if (has_suffix) {
+    LSX_TRY(check_qkv(q, sk, sv));
+    if (sk->B != q->B || sk->H != pk->H) return LSX_ERR_SHAPE;
+  }
+  {
+    const int64_t g = q->H / pk->H;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return LSX_ERR_UNSUPPORTED;
+  }
+  LSX_TRY(check_view(o));
+  if (!same_bhn_d(o, q)) return LSX_ERR_SHAPE;
+  LSX_TRY(check_row_aligned(o));
+  LSX_TRY(check_lse(lse, q));
+  if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  const int64_t parts = tree_parts(pk, has_suffix ? sk : nullptr, chunk_len);
+  if (parts > 4096) return LSX_ERR_UNSUPPORTED;
+  const size_t need = attn_decode_tree_workspace_size(q, pk, has_suffix ? sk : nullptr, chunk_len);
+  if (workspace == nullptr || workspace_bytes < need) return LSX_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  cudaStream_t s = as_stream(stream);
+  if (parts == 0) return launch_fill_empty(*o, *lse, ctx, s);
+  const float sc = resolve_scale(scale, q->D);
+  const int64_t rows = q->B * q->H;
+  float* part_o = static_cast<float*>(workspace);
+  const size_t o_bytes = static_cast<size_t>(parts * rows * q->D) * sizeof(float);
+  float* part_l = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                           ((o_bytes + 255) / 256) * 256);
+  const int64_t p_parts = ceil_div(pk->N, chunk_len);
+  if (p_parts > 0)
+    LSX_TRY(launch_decode_shared(*q, *pk, *pv, chunk_len, sc, part_o, part_l, ctx, s, 0));
+  if (has_suffix)
+    LSX_TRY(launch_decode_partials(*q, *sk, *sv, chunk_len, sc, part_o, part_l, ctx, s,
+                                   p_parts));
+  lsx_tensor po{part_o, LSX_F32, 0, q->B, q->H, 1, q->D, q->H * q->D, q->D, q->D};
+  lsx_tensor pl{part_l, LSX_F32, 0, q->B, q->H, 1, 1, q->H, 1, 1};
+  return launch_tree_merge(po, rows * q->D, pl, rows, static_cast<int>(parts), *o, *lse, ctx,
+                           s);
+}
+
 // ----------------------------------------------------------------- timing
 int lsx_timing_enable(int on) {
   g_timing.store(on != 0);
