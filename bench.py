@@ -323,6 +323,9 @@ def secondary(dev, pk):
       causal_32k_ring, noncausal_64k_heavytail
                   chunked fwd+bwd of the other two attention workloads
                   (TFLOP/s against the sustained bf16 peak)
+      decode_tree_1m_prefix
+                  shared-prefix tree decode (prefix read once for the 8
+                  branches) against plain decode over per-branch copies
       block_sparse_window_128k
                   block-sparse fwd+bwd at 128K with a sliding-window block
                   mask (only visible pairs credited)
@@ -411,6 +414,32 @@ def secondary(dev, pk):
         del x, q, k, v, d_o, o, lse, grads
         torch.cuda.empty_cache()
     out["tflops_peak"] = pk["bf16_sustained"]
+    # shared-prefix tree decoding: 8 branches x (Hq=32, Hkv=8) sharing a
+    # 1M-key prefix, each with its own 4096-key suffix; against plain decode
+    # of every branch over its own copy of prefix + suffix
+    nbr, hq_, hkv_, npre, nsuf = 8, 32, 8, 1 << 20, 4096
+    q = random_tensor((nbr, hq_, 1, 128), 101, device=dev)
+    pre_k = random_tensor((1, hkv_, npre, 128), 102, device=dev)
+    pre_v = random_tensor((1, hkv_, npre, 128), 103, device=dev)
+    sk = random_tensor((nbr, hkv_, nsuf, 128), 104, device=dev)
+    sv = random_tensor((nbr, hkv_, nsuf, 128), 105, device=dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=dev)
+    ms_tree = timed(lambda: lsx.decode_tree(q, pre_k, pre_v, sk, sv, 4096, out=o, lse=lse))
+    tree_bytes = (pre_k.numel() + pre_v.numel() + sk.numel() + sv.numel()) * 2 + 2 * q.numel() * 2
+    kc = torch.cat([pre_k.expand(nbr, -1, -1, -1), sk], dim=2)
+    vc = torch.cat([pre_v.expand(nbr, -1, -1, -1), sv], dim=2)
+    del pre_k, pre_v, sk, sv
+    ms_flat = timed(lambda: lsx.decode(q, kc, vc, 4096, out=o, lse=lse))
+    out["decode_tree_1m_prefix"] = {
+        "gbs": round(tree_bytes / ms_tree / 1e6, 1),
+        "frac": round(tree_bytes / ms_tree / 1e6 / peak, 4), "ms": round(ms_tree, 4),
+        "bytes": tree_bytes, "ms_per_branch_copies": round(ms_flat, 4),
+        "speedup": round(ms_flat / ms_tree, 2),
+        "workload": "8 branches, Hq=32, Hkv=8, shared 1,048,576-key prefix + 4096-key "
+                    "suffix each, chunk 4096"}
+    del q, kc, vc, o, lse
+    torch.cuda.empty_cache()
     # block-sparse: causal sliding window of 32 blocks (4096 keys) at 128K
     w = WORKLOADS["causal_128k_balanced"]
     x = make_inputs(w, device=dev)

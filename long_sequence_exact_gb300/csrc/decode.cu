@@ -411,9 +411,253 @@ bool launch_decode_tma(const lsx_tensor& kc, const lsx_tensor& vc, const DecodeP
   return true;
 }
 
+// ---------------------------------------------------------------------------
+// Tensor-core form for many query rows per cache (a shared prefix read by
+// the queries of several branches): R = 16 MT rows, warp w takes the 16-row
+// tile w % MT and a 16-key block of every stage (key group w / MT of
+// KG = 8 / MT); S = Q K^T and O += P V run as m16n8k16 warp MMAs with
+// fragments read by ldmatrix from 128-byte-swizzled TMA stages, P staying in
+// registers between the two products.  Per stage: 16 KG keys.
+template <int MT>
+struct DecodeMmaCfg {
+  static constexpr int kR = 16 * MT;
+  static constexpr int kKg = kWarps / MT;
+  static constexpr int kKeys = 16 * kKg;
+  static constexpr int kBox = kKeys * 128;       // one [kKeys][64] bf16 box (swizzled)
+  static constexpr int kStageBytes = 4 * kBox;   // K and V, two boxes each
+  static constexpr int kStages = kStageBytes >= 65536 ? 2 : (kStageBytes >= 32768 ? 3 : 4);
+  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+};
+
+// Shared address of the 16-byte chunk c (of 16 per 128-element row) of row r
+// in a stage tensor stored as two 128-byte-swizzled [rows][64] boxes.
+__device__ __forceinline__ uint32_t chunk_addr(uint32_t base, int box_bytes, int r, int c) {
+  return base + (c >> 3) * box_bytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+
+template <int MT>
+__global__ void __launch_bounds__(32 * (kWarps + 1), 1)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, DecodeParams p) {
+  using C = DecodeMmaCfg<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* stages = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  int* abort_flag = reinterpret_cast<int*>(empty + C::kStages);
+  __shared__ float s_m[kWarps][16];
+  __shared__ float s_l[kWarps][16];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tid4 = lane & 3;
+  const int64_t chunk = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+  const int64_t k0 = chunk * p.chunk_len;
+  const int64_t k1 = (k0 + p.chunk_len < p.N) ? k0 + p.chunk_len : p.N;
+  const int64_t n_steps = (k1 - k0 + C::kKeys - 1) / C::kKeys;
+  const WaitGuard guard{p.status, p.wait_ns, abort_flag};
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  const int mt = warp % MT, kg = warp / MT;
+  float m_a = kNegInf, m_b = kNegInf, l_a = 0.f, l_b = 0.f;  // rows gid, gid + 8
+  float o[16][4];
+#pragma unroll
+  for (int t = 0; t < 16; ++t)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[t][e] = 0.f;
+
+  if (warp == kWarps) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int64_t s = 0; s < n_steps; ++s) {
+        const int stg = static_cast<int>(s % C::kStages);
+        const uint32_t round = static_cast<uint32_t>(s / C::kStages);
+        if (round > 0 && !mbar_wait(&empty[stg], (round & 1) ^ 1, guard)) break;
+        uint8_t* dst = stages + stg * C::kStageBytes;
+        const int row = static_cast<int>(k0 + s * C::kKeys);
+        mbar_arrive_expect_tx(&full[stg], C::kStageBytes);
+        for (int half = 0; half < 2; ++half) {
+          tma_load_4d(dst + half * C::kBox, &tm_k, &full[stg], half * 64, row,
+                      static_cast<int>(hk), static_cast<int>(b));
+          tma_load_4d(dst + (2 + half) * C::kBox, &tm_v, &full[stg], half * 64, row,
+                      static_cast<int>(hk), static_cast<int>(b));
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------- compute warps
+    // Q fragments of rows 16 mt + gid (+8), all eight 16-wide K steps of d
+    uint32_t qa[8][4];
+    {
+      const int r0 = 16 * mt + gid, r1 = r0 + 8;
+      const __nv_bfloat16* q0 =
+          p.q + (p.qb0 + b + r0 / p.G) * p.q_sb + (hk * p.G + r0 % p.G) * p.q_sh;
+      const __nv_bfloat16* q1 =
+          p.q + (p.qb0 + b + r1 / p.G) * p.q_sb + (hk * p.G + r1 % p.G) * p.q_sh;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int d = 16 * ks + 2 * tid4;
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(q0 + d);
+        qa[ks][1] = *reinterpret_cast<const uint32_t*>(q1 + d);
+        qa[ks][2] = *reinterpret_cast<const uint32_t*>(q0 + d + 8);
+        qa[ks][3] = *reinterpret_cast<const uint32_t*>(q1 + d + 8);
+      }
+    }
+    const float sl2 = p.scale_log2;
+    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row of this lane
+    for (int64_t s = 0; s < n_steps; ++s) {
+      const int stg = static_cast<int>(s % C::kStages);
+      if (!mbar_wait(&full[stg], static_cast<uint32_t>(s / C::kStages) & 1, guard)) break;
+      const uint32_t kbase = smem_addr(stages + stg * C::kStageBytes);
+      const uint32_t vbase = kbase + 2 * C::kBox;
+      const int blk = 16 * kg;  // first key of this warp's block in the stage
+      // S[16 x 16] = Q K^T: matrices (keys 0-7 | 8-15) x (d chunk 2ks | 2ks+1)
+      float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint32_t kb[4];
+        ldsm_x4(chunk_addr(kbase, C::kBox, blk + (mi >> 1) * 8 + ri, 2 * ks + (mi & 1)), kb);
+        mma_16816(sc[0], qa[ks], kb[0], kb[1]);
+        mma_16816(sc[1], qa[ks], kb[2], kb[3]);
+      }
+      // online softmax of rows gid (elements 0, 1) and gid + 8 (2, 3)
+      const int64_t key0 = k0 + s * C::kKeys + blk;
+      float mx_a = kNegInf, mx_b = kNegInf;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int64_t key = key0 + nt * 8 + 2 * tid4 + (e & 1);
+          const float v = key < k1 ? sc[nt][e] * sl2 : kNegInf;
+          sc[nt][e] = v;
+          if (e < 2) mx_a = fmaxf(mx_a, v); else mx_b = fmaxf(mx_b, v);
+        }
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 1));
+      mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, 2));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 1));
+      mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, 2));
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float al_a = (m_a == kNegInf) ? 0.f : ex2(m_a - mn_a);
+      const float al_b = (m_b == kNegInf) ? 0.f : ex2(m_b - mn_b);
+      const float mu_a = (mn_a == kNegInf) ? 0.f : mn_a;
+      const float mu_b = (mn_b == kNegInf) ? 0.f : mn_b;
+      m_a = mn_a;
+      m_b = mn_b;
+      float ps_a = 0.f, ps_b = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float pe = ex2(sc[nt][e] - (e < 2 ? mu_a : mu_b));
+          sc[nt][e] = pe;
+          if (e < 2) ps_a += pe; else ps_b += pe;
+        }
+      l_a = l_a * al_a + ps_a;
+      l_b = l_b * al_b + ps_b;
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        o[t][0] *= al_a; o[t][1] *= al_a;
+        o[t][2] *= al_b; o[t][3] *= al_b;
+      }
+      // P as the A fragment of O += P V (k = the 16 keys)
+      uint32_t pa[4];
+      pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+      pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+      pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+      pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+      // V fragments: transposed matrices (keys 0-7 | 8-15) x (d chunk t | t+1)
+#pragma unroll
+      for (int t2 = 0; t2 < 8; ++t2) {
+        uint32_t vb[4];
+        ldsm_x4_t(chunk_addr(vbase, C::kBox, blk + (mi & 1) * 8 + ri, 2 * t2 + (mi >> 1)), vb);
+        mma_16816(o[2 * t2], pa, vb[0], vb[1]);
+        mma_16816(o[2 * t2 + 1], pa, vb[2], vb[3]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stg]);  // this warp is done with the stage
+    }
+    // row sums over the four lanes that share a row
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 1);
+    l_a += __shfl_xor_sync(0xffffffffu, l_a, 2);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 1);
+    l_b += __shfl_xor_sync(0xffffffffu, l_b, 2);
+  }
+  // merge the KG warps of each 16-row tile; the per-warp O rows reuse the
+  // stage memory once every stage has been consumed
+  __syncthreads();
+  float* s_o = reinterpret_cast<float*>(stages);  // [kWarps][16][128]
+  if (warp < kWarps) {
+    if (tid4 == 0) {
+      s_m[warp][gid] = m_a;
+      s_m[warp][gid + 8] = m_b;
+      s_l[warp][gid] = l_a;
+      s_l[warp][gid + 8] = l_b;
+    }
+#pragma unroll
+    for (int t = 0; t < 16; ++t) {
+      const int d = 8 * t + 2 * tid4;
+      s_o[(warp * 16 + gid) * 128 + d] = o[t][0];
+      s_o[(warp * 16 + gid) * 128 + d + 1] = o[t][1];
+      s_o[(warp * 16 + gid + 8) * 128 + d] = o[t][2];
+      s_o[(warp * 16 + gid + 8) * 128 + d + 1] = o[t][3];
+    }
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < C::kR * 128; idx += blockDim.x) {
+    const int r = idx / 128, d = idx % 128;
+    const int tile = r / 16, rr = r % 16;
+    float mm = kNegInf;
+    for (int w = tile; w < kWarps; w += MT) mm = fmaxf(mm, s_m[w][rr]);
+    float tot = 0.f, acc = 0.f;
+    if (mm != kNegInf) {
+      for (int w = tile; w < kWarps; w += MT) {
+        const float f = (s_m[w][rr] == kNegInf) ? 0.f : ex2(s_m[w][rr] - mm);
+        tot += s_l[w][rr] * f;
+        acc += s_o[(w * 16 + rr) * 128 + d] * f;
+      }
+    }
+    const int64_t row = (p.qb0 + b + r / p.G) * p.Hq + hk * p.G + r % p.G;
+    const int64_t part = p.part0 + chunk;
+    p.part_o[(part * p.rows + row) * 128 + d] = (tot > 0.f) ? acc / tot : 0.f;
+    if (d == 0)
+      p.part_l[part * p.rows + row] = (tot > 0.f) ? (mm + lg2(tot)) * kLn2 : kNegInf;
+  }
+}
+
+template <int MT>
+bool launch_decode_mma(const lsx_tensor& kc, const lsx_tensor& vc, const DecodeParams& p,
+                       dim3 grid, cudaStream_t s) {
+  using C = DecodeMmaCfg<MT>;
+  CUtensorMap tk, tv;
+  if (!make_map_bf16_4d(&tk, kc.data, kc.B, kc.H, kc.N, kc.D, kc.stride_b, kc.stride_h,
+                        kc.stride_n, C::kKeys) ||
+      !make_map_bf16_4d(&tv, vc.data, vc.B, vc.H, vc.N, vc.D, vc.stride_b, vc.stride_h,
+                        vc.stride_n, C::kKeys))
+    return false;
+  if (cudaFuncSetAttribute(decode_mma_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::kSmem) != cudaSuccess)
+    return false;
+  decode_mma_kernel<MT><<<grid, 32 * (kWarps + 1), C::kSmem, s>>>(tk, tv, p);
+  return true;
+}
+
 // Rows per CTA R (a multiple of 2 up to 64): picks the (GW, RG) instance.
+// Sixteen rows or more take the tensor-core form.
 bool launch_decode_rows(int64_t R, const lsx_tensor& kc, const lsx_tensor& vc,
                         const DecodeParams& p, dim3 grid, cudaStream_t s) {
+  switch (R) {
+    case 16: return launch_decode_mma<1>(kc, vc, p, grid, s);
+    case 32: return launch_decode_mma<2>(kc, vc, p, grid, s);
+    case 64: return launch_decode_mma<4>(kc, vc, p, grid, s);
+    default: break;
+  }
   switch (R) {
     case 2: return launch_decode_tma<2, 1>(kc, vc, p, grid, s);
     case 4: return launch_decode_tma<4, 1>(kc, vc, p, grid, s);

@@ -31,6 +31,7 @@ def oracle_tree(q, pk, pv, sk, sv):
 
 @pytest.mark.parametrize("branches,g,np_,ns", [
     (8, 4, 20000, 1000),   # 32 query rows per kv head against the prefix
+    (4, 4, 10000, 100),    # 16 rows: one 16-row warp tile, eight key groups
     (3, 4, 5000, 300),     # ragged branch groups (2 + 1)
     (5, 1, 4096, 700),     # MHA, odd branch count
     (16, 8, 9000, 0),      # 128 rows: two groups of 8 branches, no suffixes
@@ -62,5 +63,8 @@ def test_decode_tree_equals_plain_decode_on_the_concatenated_cache():
     kc = torch.cat([pk.expand(b, -1, -1, -1), sk], dim=2).contiguous()
     vc = torch.cat([pv.expand(b, -1, -1, -1), sv], dim=2).contiguous()
     o2, l2 = lsx.decode(q, kc, vc, 4096, out_dtype=torch.float32)
-    assert float((o - o2).abs().max()) < 1e-5
+    # 16 query rows per kv head take the tensor-core prefix kernel, which
+    # rounds P to bf16 before the P V product (the plain decode keeps it in
+    # f32): O agrees to that rounding, LSE (from the f32 scores) closely
+    assert float((o - o2).abs().max()) < 1e-3
     assert float((lse - l2).abs().max()) < 1e-5
