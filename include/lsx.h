@@ -153,14 +153,17 @@ int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
  *   outputs to sum over many chunk pairs).
  * Workspace (256-byte aligned): at least attn_chunk_bwd_min_workspace_size
  * bytes (the row sums delta_i = <dO_i, O_i>, 4 bytes per query row).  With
- * attn_chunk_bwd_workspace_size bytes (bf16 inputs) two more things are
- * written there first: a key-contiguous copy of K, which the dQ product
- * reads at the tensor cores' faster operand layout, and 16 bytes per query
- * row of row statistics (-LSE/scale and -delta as bf16 triples), which the
- * dK/dV kernel adds to its score products on the tensor cores instead of
- * per element.  With less, K is read as stored and the statistics are
- * applied per element.  Both give results within the documented tolerance
- * of each other (the statistics triples carry 24 significant bits).
+ * attn_chunk_bwd_workspace_size bytes (bf16 inputs) more is kept there:
+ * 16 bytes per query row of row statistics (-LSE/scale and -delta as bf16
+ * triples), which the dK/dV products add to their score tiles on the tensor
+ * cores instead of per element, and one scratch region used EITHER as the
+ * fp32 dQ accumulator of the fused D = 128 kernel (4 bytes x B x Hq x Lq x
+ * D; see lsx_set_deterministic) OR as a key-contiguous copy of K, which the
+ * separate dQ kernel reads at the tensor cores' faster operand layout.
+ * With less, the statistics are applied per element, K is read as stored,
+ * and the fused kernel runs only when dq is f32 (it then adds into dq
+ * directly).  All forms give results within the documented tolerance of
+ * each other (the statistics triples carry 24 significant bits).
  * ---------------------------------------------------------------------- */
 size_t attn_chunk_bwd_min_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
 size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k);
@@ -316,6 +319,18 @@ const char* lsx_status_string(int code);
  * before the kernel gives up, records LSX_ERR_TIMEOUT and exits.  0 restores
  * the default (10 s).  Process-wide; affects launches made after the call. */
 void lsx_set_wait_limit_ns(uint64_t ns);
+
+/* Backward reduction order.  on == 0 (the default): for D = 128 one kernel
+ * computes dK, dV and dQ together and adds each key tile's contribution to
+ * dQ into an fp32 accumulator with global atomic adds, so dQ's rounding
+ * depends on the order in which those adds land (results agree with the
+ * deterministic mode within the documented tolerance, not bit for bit).
+ * on != 0: dQ is computed by a second kernel in which every dQ row is owned
+ * by one thread block, and repeated calls on the same inputs give identical
+ * bytes (slower: the score tiles are rebuilt a second time).  dK and dV are
+ * identical between calls in both modes.  Process-wide; affects calls made
+ * after it. */
+void lsx_set_deterministic(int on);
 
 /* Launches one block that waits on an mbarrier nothing will ever complete,
  * under the current wait limit, so that callers can check that a bounded wait

@@ -19,6 +19,7 @@ from .attention import (  # noqa: F401
     merge,
     schedule_stats,
     selftest_bounded_wait,
+    set_deterministic,
     set_wait_limit_ns,
     status_string,
     sync_status,
@@ -31,6 +32,6 @@ __all__ = [
     "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "block_sparse_fwd",
     "block_sparse_bwd", "merge", "tree_merge",
     "decode", "decode_tree", "decode_workspace_size", "schedule_stats", "selftest_bounded_wait",
-    "set_wait_limit_ns", "status_string", "sync_status", "version", "chunked_attention",
+    "set_deterministic", "set_wait_limit_ns", "status_string", "sync_status", "version", "chunked_attention",
     "ChunkedAttention",
 ]

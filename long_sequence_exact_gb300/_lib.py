@@ -80,6 +80,7 @@ SIGNATURES = {
     "lsx_sync_status": (_INT, [_VP]),
     "lsx_status_string": (ctypes.c_char_p, [_INT]),
     "lsx_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "lsx_set_deterministic": (None, [_INT]),
     "lsx_selftest_bounded_wait": (_INT, [_VP]),
     "lsx_schedule_stats": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, ctypes.POINTER(_I64)]),
     "lsx_version": (ctypes.c_char_p, []),

@@ -262,6 +262,13 @@ def set_wait_limit_ns(ns: int) -> None:
     load().lsx_set_wait_limit_ns(int(ns))
 
 
+def set_deterministic(on: bool) -> None:
+    """Select the backward's dQ reduction order (lsx_set_deterministic):
+    False (default) = fused dK/dV/dQ kernel adding dQ with fp32 atomics,
+    True = owner-computes dQ kernel, bitwise repeatable."""
+    load().lsx_set_deterministic(1 if on else 0)
+
+
 def selftest_bounded_wait() -> None:
     check(load().lsx_selftest_bounded_wait(stream_handle()), "lsx_selftest_bounded_wait")
 

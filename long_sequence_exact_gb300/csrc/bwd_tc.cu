@@ -8,8 +8,7 @@
 // dS_ij = P_ij (dO_i.v_j - delta_i):
 //   dV = P^T dO,   dK = scale dS^T Q,   dQ = scale dS K.
 //
-// Two persistent kernels, both deterministic (every output tile is owned by
-// exactly one CTA; no atomics):
+// Persistent kernels:
 //  * dkdv_kernel, key-tile-major: a work item is one 128-row key/value tile
 //    of one (batch, kv head); it walks every query tile (of every query head
 //    of the group) that sees it:
@@ -18,7 +17,16 @@
 //      grad warps: P^T, dS^T -> bf16 back into TMEM (inside [0,128), [128,256))
 //      dV  += P^T dO_i    (TS, dO_i MN-major)          TMEM [256,256+D)
 //      dK  += dS^T Q_i    (TS, Q_i MN-major)           TMEM [384,384+D)
-//  * dq_kernel, query-tile-major: a work item is one 128-row query tile; it
+//    With kDq (D = 128) it also forms dQ: once dV has read dO_i for the
+//    last time, the grad warps write dS^T into dO_i's shared-memory slot and
+//      dQ_i^T = K^T dS^T  (SS, both MN-major)          TMEM [128,256)
+//    which they read back (the next dP^T waits only for that), scale and
+//    stage as fp32 [query][d] rows in the now dead Q_i / dO_i slots; one
+//    thread of warp 2 adds the staged tile into the fp32 dQ accumulator
+//    with bulk TMA reduce-adds and frees the slots for the next loads once
+//    the TMA unit has read them.  dK and dV stay owned by one CTA each; dQ's
+//    summation order varies between runs.
+//  * dq_kernel (the deterministic form of dQ), query-tile-major: a work item is one 128-row query tile; it
 //    walks every visible key tile:
 //      S  = Q K_j^T, dP = dO V_j^T (SS)                TMEM [0,128), [128,256)
 //      grad warps: dS -> bf16 into TMEM (inside [128,256))
@@ -76,6 +84,9 @@ struct BwdParams {
   const int32_t* row_list;  // stride n_ktiles
   const int32_t* col_count;
   const int32_t* col_list;  // stride n_qtiles
+  // fused dQ: fp32 accumulator and its strides (elements)
+  float* dq_acc;
+  int64_t acc_sb, acc_sh, acc_sn;
 };
 
 // TMEM column (relative to the 128-column fp32 tile) of the packed bf16
@@ -222,6 +233,7 @@ struct DkdvSmem {
   uint64_t st_full[2], st_empty[2];
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_full, p_full, dkv_done;
+  uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ only
   uint32_t tmem_base;
   int abort;
 };
@@ -302,7 +314,7 @@ __host__ __device__ constexpr uint64_t seq_b_step(int kk) {
 // -delta) to every score of each query column; the grad warps then need
 // neither the LSE nor delta.  Without kRS warp 0 gathers both into shared
 // memory and the grad warps apply them per element.
-template <int D, bool kRS>
+template <int D, bool kRS, bool kDq>
 __global__ void __launch_bounds__(640, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
@@ -311,6 +323,7 @@ __global__ void __launch_bounds__(640, 1)
                 const __grid_constant__ CUtensorMap tm_rs,
                 const __grid_constant__ CUtensorMap tm_ones, const BwdParams p) {
   using Sm = DkdvSmem<D>;
+  static_assert(!kDq || D == 128, "fused dQ: the dQ^T tile spans TMEM lanes 0..127");
   constexpr int kTile = 128 * D * 2;
   constexpr int kQoStages = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -333,6 +346,11 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.p_full, 512);
     mbar_init(&sm.dkv_done, 1);
+    mbar_init(&sm.dv_done, 1);
+    mbar_init(&sm.ds_full, 512);
+    mbar_init(&sm.dq_full, 1);
+    mbar_init(&sm.dq_drained, 512);
+    mbar_init(&sm.stage_full, 512);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -407,8 +425,9 @@ __global__ void __launch_bounds__(640, 1)
       // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
-      uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0;
-      bool issued = false;
+      constexpr uint32_t kIdQ = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T = K^T dS^T
+      uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0, ds_phase = 0, dr_phase = 0;
+      bool issued = false, dq_pending = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
       // selector and statistics tiles: 16 core matrices of 8 rows x 16 bytes
       // along M/N (128 bytes apart); the K step's second core matrix re-reads
@@ -430,22 +449,49 @@ __global__ void __launch_bounds__(640, 1)
           tc_fence_after();
           const uint32_t q_addr = smem_addr(sm.q[qs]);
           const uint32_t o_addr = smem_addr(sm.d_o[qs]);
+          const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
           mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
-          if constexpr (kRS) {
-            const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
-            mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
-            mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
-            mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
-          } else {
-            mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+          if constexpr (kRS) mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
+          if (kDq && dq_pending) {  // dP^T reuses the columns of the last dQ^T
+            if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
+            dr_phase ^= 1;
+            tc_fence_after();
           }
+          mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+          if constexpr (kRS) mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
           mma_commit(&sm.s_full);
           issued = true;
           if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
           p_phase ^= 1;
           const uint32_t bq = q_addr, bo = o_addr;
           tc_fence_after();
-          {
+          if constexpr (kDq) {
+            const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
+            const uint32_t acc0 = s > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG,
+                     kk > 0 ? 1u : acc0);
+            mma_commit(&sm.dv_done);  // dO_i has been read for the last time
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
+                     kk > 0 ? 1u : acc0);
+            if (!mbar_wait(&sm.ds_full, ds_phase, guard)) { ok = false; break; }
+            ds_phase ^= 1;
+            tc_fence_after();
+            // A = K^T (d x keys) and B = dS^T as [query][key], both read from
+            // [key][*] tiles, MN-major; the dS^T columns just read by dK are
+            // overwritten only after it (one thread's MMAs run in issue order)
+            const uint64_t ka0 = sdesc_sw128(k_addr, 128 * 128, 1024);
+            const uint64_t db0 = sdesc_sw128(bo, 128 * 128, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(tmem + 128, ka0 + mnmajor_step(kk), db0 + mnmajor_step(kk), kIdQ,
+                     kk > 0 ? 1u : 0u);
+            mma_commit(&sm.dq_full);
+            dq_pending = true;
+          } else {
             const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
             const uint32_t acc0 = s > 0 ? 1u : 0u;
 #pragma unroll
@@ -457,7 +503,7 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
           mma_commit(&sm.dkv_done);
-          mma_commit(&sm.st_empty[qs]);
+          if constexpr (!kDq) mma_commit(&sm.st_empty[qs]);  // (kDq: the reducer frees it)
           if (++qs == kQoStages) { qs = 0; qph ^= 1; }
         }
         if (!ok) break;
@@ -467,6 +513,47 @@ __global__ void __launch_bounds__(640, 1)
         mma_commit(&sm.final_bar);
         drain_wait(&sm.final_bar, 0, p.wait_ns);
       }
+    } else if (kDq && warp == 2 && lane == 0) {
+      // ------------------------------------------ dQ reducer (fused form)
+      // Step by step: wait for the grad warps' staged scale * dQ_i (fp32
+      // rows of 128; queries 0..63 in the Q_i slot, 64..127 in the dO_i
+      // slot), add it into the accumulator with bulk reduce-adds, and free
+      // both slots once the TMA unit has read them.
+      uint32_t slot = 0, sf_phase = 0;
+      bool any = false;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DkdvItem x = dkdv_item(p, it);
+        bool ok = true;
+        for (int64_t s = 0; s < x.n_i; ++s) {
+          int64_t h, i;
+          dkdv_step(p, x, s, h, i);
+          if (!mbar_wait(&sm.stage_full, sf_phase, guard)) { ok = false; break; }
+          sf_phase ^= 1;
+          for (int half = 0; half < 2; ++half) {
+            const int64_t q0 = i * 128 + 64 * half;
+            int64_t rows = p.Lq - q0;
+            if (rows <= 0) continue;
+            if (rows > 64) rows = 64;
+            const uint8_t* src = reinterpret_cast<const uint8_t*>(half ? sm.d_o[slot] : sm.q[slot]);
+            float* dst = p.dq_acc + x.b * p.acc_sb + h * p.acc_sh + q0 * p.acc_sn;
+            if (p.acc_sn == 128) {
+              bulk_reduce_add_f32(dst, src, static_cast<uint32_t>(rows * 512));
+            } else {
+              for (int64_t rr = 0; rr < rows; ++rr)
+                bulk_reduce_add_f32(dst + rr * p.acc_sn, src + rr * 512, 512u);
+            }
+          }
+          bulk_commit();
+          bulk_wait_read();
+          any = true;
+          mbar_arrive(&sm.st_empty[slot]);
+          if (++slot == kQoStages) slot = 0;
+        }
+        if (!ok) break;
+      }
+      if (any) bulk_wait_all();
     }
   } else {
     regs_inc<104>();
@@ -477,7 +564,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const uint32_t tS = tmem + lane_base + 32 * qtr;        // S^T / P^T
     const uint32_t tP = tmem + lane_base + 128 + 32 * qtr;  // dP^T / dS^T
-    uint32_t ls = 0, lph = 0, s_phase = 0;
+    uint32_t ls = 0, lph = 0, s_phase = 0, dq_phase = 0, gs = 0;
     uint32_t d_count = 0;
     const float sl2 = p.scale_log2;
     const float2 sc2 = make_float2(sl2, sl2);
@@ -488,8 +575,8 @@ __global__ void __launch_bounds__(640, 1)
       const int64_t key_abs = p.kv_off + x.j * 128 + row;
       bool ok = true;
       for (int64_t s = 0; s < x.n_i; ++s) {
-        int64_t h_unused, i;
-        dkdv_step(p, x, s, h_unused, i);
+        int64_t h, i;
+        dkdv_step(p, x, s, h, i);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
@@ -505,12 +592,12 @@ __global__ void __launch_bounds__(640, 1)
         }
         const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[ls][32 * qtr]);
         const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[ls][32 * qtr]);
+        uint32_t pk[16], dk[16];
         if constexpr (kRS) {
           // the scores already hold S - LSE/scale and dP - delta; only
           // tiles that straddle the diagonal for this warp need the mask
           const bool need_mask =
               p.causal && p.kv_off + x.j * 128 + quad * 32 + 31 > p.q_off + i * 128 + 32 * qtr;
-          uint32_t pk[16], dk[16];
           if (need_mask)
             grad_rows_rs<true>(us, ud, sc2, cmin, pk, dk);
           else
@@ -519,7 +606,6 @@ __global__ void __launch_bounds__(640, 1)
           tmem_st16(tP, dk);
         } else {
           constexpr int cc = 0;
-          uint32_t pk[16], dk[16];
 #pragma unroll
           for (int e4 = 0; e4 < 8; ++e4) {
             const float4 l4 = l2v[cc * 8 + e4];
@@ -551,6 +637,53 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_before();
         mbar_arrive(&sm.p_full);
         ++d_count;
+        if constexpr (kDq) {
+          // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle,
+          // the layout a TMA load of such a tile produces) into the slot of
+          // dO_i, once the dV product has finished reading it
+          // (the packed pairs are read back from TMEM rather than kept live
+          // in registers across the wait)
+          if (!mbar_wait(&sm.dv_done, dq_phase, guard)) { ok = false; break; }
+          {
+            uint32_t w[16];
+            tmem_ld16_sync(tP, w);
+            uint8_t* line = reinterpret_cast<uint8_t*>(sm.d_o[gs]) + (qtr >> 1) * 16384 + row * 128;
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int ch = (qtr & 1) * 4 + c4;  // 16-byte chunk (8 queries) in the line
+              *reinterpret_cast<uint4*>(line + ((ch ^ (row & 7)) << 4)) =
+                  make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+            }
+          }
+          fence_proxy_async_smem();
+          tc_fence_before();  // the TMEM read above precedes dQ^T's writes there
+          mbar_arrive(&sm.ds_full);
+          const uint32_t gs_prev = gs;
+          if (++gs == 2) gs = 0;
+          // dQ_i^T: lane = dimension quad * 32 + lane, columns = this
+          // quarter's 32 queries; read it, release the columns, then add
+          // scale * dQ^T into the accumulator (one 128-byte row segment per
+          // warp instruction)
+          if (!mbar_wait(&sm.dq_full, dq_phase, guard)) { ok = false; break; }
+          dq_phase ^= 1;
+          tc_fence_after();
+          uint32_t u[32];
+          tmem_ld32(tmem + lane_base + 128 + 32 * qtr, u);
+          tmem_ld_wait32(u);
+          tc_fence_before();
+          mbar_arrive(&sm.dq_drained);
+          // stage scale * dQ^T as [query][d] fp32 rows of 512 bytes: the
+          // dQ^T MMA (complete) was the last reader of both slots; each warp
+          // store covers 128 consecutive bytes of one row
+          {
+            float* stage = reinterpret_cast<float*>(qtr < 2 ? sm.q[gs_prev] : sm.d_o[gs_prev]) +
+                           (qtr & 1) * 32 * 128 + row;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) stage[e * 128] = __uint_as_float(u[e]) * p.scale;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(&sm.stage_full);
+        }
       }
       if (!ok) break;
       // epilogue: half 0 writes dV, half 1 writes dK (times scale)
@@ -892,6 +1025,40 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
+// dq (bf16 or f32 view, D = 128) = acc (dense fp32 [B*Hq*Lq][128]),
+// optionally added to what dq holds; four columns per thread.
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, void* dq,
+                                                         int f32, int64_t sb, int64_t sh,
+                                                         int64_t sn, int64_t Hq, int64_t Lq,
+                                                         int64_t total4, int accumulate) {
+  for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total4;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t rowi = t >> 5;
+    const int64_t col = (t & 31) * 4;
+    const int64_t n = rowi % Lq, bh = rowi / Lq;
+    const int64_t off = (bh / Hq) * sb + (bh % Hq) * sh + n * sn + col;
+    float4 a = reinterpret_cast<const float4*>(acc)[t];
+    if (f32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dq) + off);
+      if (accumulate) {
+        const float4 o = *d;
+        a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+      }
+      *d = a;
+    } else {
+      uint2* d = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dq) + off);
+      if (accumulate) {
+        const uint2 o = *d;
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&o.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&o.y);
+        a.x += __low2float(lo); a.y += __high2float(lo);
+        a.z += __low2float(hi); a.w += __high2float(hi);
+      }
+      *d = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+    }
+  }
+}
+
 bool map_rows(CUtensorMap* m, const lsx_tensor& t) {
   return make_map_bf16_4d(m, t.data, t.B, t.H, t.N, t.D, t.stride_b, t.stride_h, t.stride_n,
                           128);
@@ -914,7 +1081,12 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                     float scale, const lsx_tensor& dq, const lsx_tensor& dk,
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
                     cudaStream_t s, const BlockLists* bl) {
-  const bool tr = cp.kt != nullptr;
+  // fused dK/dV/dQ: D = 128, not in deterministic mode, and somewhere to
+  // add dQ into (the fp32 accumulator in the workspace, or an f32 dq)
+  const bool fused = D == 128 && !ctx.deterministic &&
+                     (cp.dq_acc != nullptr || dq.dtype == LSX_F32);
+  const bool direct = fused && dq.dtype == LSX_F32;  // add straight into dq
+  const bool tr = !fused && cp.kt != nullptr;
   const bool rs = cp.stats.rows != nullptr;
   CUtensorMap tq, tk, tv, tdo, tkt, trs, tones;
   if (!map_rows(&tq, q) || !map_rows(&tk, k) || !map_rows(&tv, v) || !map_rows(&tdo, d_o))
@@ -954,12 +1126,50 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.row_list = bl ? bl->row_list : nullptr;
   p.col_count = bl ? bl->col_count : nullptr;
   p.col_list = bl ? bl->col_list : nullptr;
+  p.dq_acc = nullptr;
+  p.acc_sb = p.acc_sh = p.acc_sn = 0;
 
-  // dK, dV: items (key tile, b, kv head)
+  // dK, dV (and dQ): items (key tile, b, kv head)
   p.n_items = p.n_ktiles * q.B * k.H;
+  if constexpr (D == 128) if (fused) {
+    if (direct) {
+      p.dq_acc = static_cast<float*>(dq.data);
+      p.acc_sb = dq.stride_b; p.acc_sh = dq.stride_h; p.acc_sn = dq.stride_n;
+      if (!accumulate) {
+        const int rc = launch_zero(dq, ctx, s);
+        if (rc != LSX_OK) return rc;
+      }
+    } else {
+      p.dq_acc = cp.dq_acc;
+      p.acc_sn = D; p.acc_sh = q.N * D; p.acc_sb = q.H * q.N * D;
+      if (cudaMemsetAsync(cp.dq_acc, 0, static_cast<size_t>(q.B * q.H * q.N * D) * sizeof(float),
+                          s) != cudaSuccess)
+        return LSX_ERR_LAUNCH;
+    }
+    const size_t smem = sizeof(DkdvSmem<D>) + 1024;
+    auto kern = rs ? dkdv_kernel<D, true, true> : dkdv_kernel<D, false, true>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return LSX_ERR_LAUNCH;
+    const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    timing_begin(kKidBwdFused, s);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, p);
+    timing_end(kKidBwdFused, s);
+    if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
+    if (direct) return LSX_OK;
+    const int64_t total4 = q.B * q.H * q.N * (D / 4);
+    int64_t blocks = (total4 + 255) / 256;
+    if (blocks > 8 * ctx.sm_count) blocks = 8 * ctx.sm_count;
+    timing_begin(kKidDqConvert, s);
+    dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        cp.dq_acc, dq.data, dq.dtype == LSX_F32, dq.stride_b, dq.stride_h, dq.stride_n, q.H, q.N,
+        total4, accumulate);
+    timing_end(kKidDqConvert, s);
+    return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+  }
   {
     const size_t smem = sizeof(DkdvSmem<D>) + 1024;
-    auto kern = rs ? dkdv_kernel<D, true> : dkdv_kernel<D, false>;
+    auto kern = rs ? dkdv_kernel<D, true, false> : dkdv_kernel<D, false, false>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
@@ -988,21 +1198,37 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
 
 }  // namespace
 
-// Scratch behind delta: [key-contiguous K][selector tiles, 4 KiB][row
-// statistics, 16 bytes per query row].
-size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k) {
-  const size_t kt = (transposed_bytes(k) + 255) / 256 * 256;
+// Scratch behind delta: [selector tiles, 4 KiB][row statistics, 16 bytes
+// per query row][one region holding either the fp32 dQ accumulator (D = 128)
+// or the key-contiguous copy of K].
+namespace {
+size_t stats_bytes(const lsx_tensor& q) {
   const size_t rows = static_cast<size_t>(q.B * q.H * q.N);
-  return kt + (2 * 128 * 16 + rows * 16 + 255) / 256 * 256;
+  return (2 * 128 * 16 + rows * 16 + 255) / 256 * 256;
+}
+size_t scratch_bytes(const lsx_tensor& q, const lsx_tensor& k) {
+  size_t n = transposed_bytes(k);
+  if (q.D == 128) {
+    const size_t acc = static_cast<size_t>(q.B * q.H * q.N) * 128 * sizeof(float);
+    if (acc > n) n = acc;
+  }
+  return (n + 255) / 256 * 256;
+}
+}  // namespace
+
+size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k) {
+  return stats_bytes(q) + scratch_bytes(q, k);
 }
 
 BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base) {
-  (void)q;
+  (void)k;
   BwdCopies c;
-  c.kt = base;
-  char* st = static_cast<char*>(base) + (transposed_bytes(k) + 255) / 256 * 256;
+  char* st = static_cast<char*>(base);
   c.stats.ones = st;
   c.stats.rows = st + 2 * 128 * 16;
+  char* scratch = st + stats_bytes(q);
+  c.kt = scratch;
+  if (q.D == 128) c.dq_acc = reinterpret_cast<float*>(scratch);
   return c;
 }
 

@@ -14,6 +14,7 @@ struct DeviceCtx {
   int sm_count;
   int* status;        // device address of this device's status word
   uint64_t wait_ns;   // bound of every device-side wait
+  int deterministic;  // backward: owner-computes dQ (no fp32 reductions)
 };
 
 // Fills ctx for the current device; returns LSX_OK or LSX_ERR_DEVICE.
@@ -23,7 +24,8 @@ int device_ctx(DeviceCtx* ctx);
 // recorded on the launching stream around every launch of kernel `kid`.
 enum KernelId {
   kKidFwdTc = 0, kKidDkdv, kKidDq, kKidRowDot, kKidMerge, kKidTreeMerge,
-  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidTranspose, kKidBlockLists, kKidCount
+  kKidDecode, kKidSimtFwd, kKidSimtBwd, kKidFill, kKidTranspose, kKidBlockLists,
+  kKidBwdFused, kKidDqConvert, kKidCount
 };
 
 // Sequence-contiguous copies (layout.cu): a bf16 [B, H, N, D] view is
@@ -123,15 +125,21 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& lse, int accumulate, void* vt,
                   const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
-// tcgen05 tensor-core backward (bf16 inputs).  With copies.kt non-NULL, a
-// key-contiguous copy of K is written there first and the dQ product reads
-// it K-major; with NULL the K tiles are read as stored (MN-major), which
-// needs no scratch beyond delta.  With copies.stats.rows non-NULL (written
-// by launch_row_dot beforehand) the dK/dV kernel takes -LSE/scale and
-// -delta into its score products as one extra rank-1 K step instead of
-// applying them per element.
+// tcgen05 tensor-core backward (bf16 inputs).  For D = 128 (unless the
+// deterministic mode is set) one kernel computes dK, dV and dQ, adding each
+// key tile's dQ contribution into an fp32 accumulator: copies.dq_acc
+// (dense [B, Hq, Lq, D], zeroed and converted to dq by the launcher) or,
+// when dq itself is f32, dq directly.  Otherwise two kernels own their
+// outputs: with copies.kt non-NULL, a key-contiguous copy of K is written
+// there first and the dQ product reads it K-major; with NULL the K tiles
+// are read as stored (MN-major), which needs no scratch beyond delta.  With
+// copies.stats.rows non-NULL (written by launch_row_dot beforehand) the
+// dK/dV kernel takes -LSE/scale and -delta into its score products as one
+// extra rank-1 K step instead of applying them per element.  kt and dq_acc
+// share one scratch region; a launch uses at most one of them.
 struct BwdCopies {
   void* kt = nullptr;
+  float* dq_acc = nullptr;
   RowStats stats;
 };
 size_t bwd_tc_copies_bytes(const lsx_tensor& q, const lsx_tensor& k);

@@ -23,6 +23,7 @@ namespace {
 
 constexpr uint64_t kDefaultWaitNs = 10ull * 1000 * 1000 * 1000;  // 10 s
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int> g_deterministic{0};
 
 struct DevCache {
   bool ready = false;
@@ -35,7 +36,8 @@ std::vector<DevCache> g_devs;
 // ------------------------------------------------------- kernel timing
 const char* const kKernelNames[kKidCount] = {
     "fwd_tc", "bwd_dkdv_tc", "bwd_dq_tc", "bwd_row_dot", "merge", "tree_merge",
-    "decode_partials", "simt_fwd", "simt_bwd", "fill", "transpose", "block_lists"};
+    "decode_partials", "simt_fwd", "simt_bwd", "fill", "transpose", "block_lists",
+    "bwd_fused_tc", "bwd_dq_convert"};
 std::atomic<bool> g_timing{false};
 struct TimedLaunch {
   int kid;
@@ -99,6 +101,7 @@ int device_ctx(DeviceCtx* ctx) {
   ctx->sm_count = dc.sm_count;
   ctx->status = dc.status;
   ctx->wait_ns = g_wait_ns.load();
+  ctx->deterministic = g_deterministic.load();
   return LSX_OK;
 }
 
@@ -198,6 +201,8 @@ const char* lsx_status_string(int code) {
 void lsx_set_wait_limit_ns(uint64_t ns) {
   g_wait_ns.store(ns == 0 ? kDefaultWaitNs : ns);
 }
+
+void lsx_set_deterministic(int on) { g_deterministic.store(on != 0 ? 1 : 0); }
 
 int lsx_sync_status(lsx_stream_t stream) {
   DeviceCtx ctx;

@@ -260,6 +260,21 @@ LSX_DEV void tmem_ld_wait32(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns load, waited for in the same
+// call (the registers are tied to the wait).
+LSX_DEV void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]),
+        "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]),
+        "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Compiler-only fence: uses of r cannot move above an earlier
 // tmem_ld_wait32 (lets several loads share one wait).
 LSX_DEV void reg_fence32(uint32_t (&r)[32]) {
@@ -305,6 +320,26 @@ LSX_DEV void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
 LSX_DEV void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+
+// Makes this thread's shared-memory stores visible to the async proxy
+// (tensor-core operand reads) once a later barrier orders the two.
+LSX_DEV void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk asynchronous fp32 add of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned) from shared to global memory, performed by the TMA unit
+// at L2; grouped with bulk_commit and waited for with bulk_wait_read (source
+// may be reused) or bulk_wait_all (writes done).
+LSX_DEV void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
+  asm volatile(
+      "cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+      "r"(smem_addr(src)), "r"(bytes)
+      : "memory");
+}
+LSX_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+LSX_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+LSX_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Per-warpgroup register budget changes (all 4 warps of a warpgroup execute
 // the same call).  The increases drawn by some warpgroups must fit in what

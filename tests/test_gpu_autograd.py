@@ -34,5 +34,9 @@ def test_autograd_matches_oracle_and_recompute_form(causal):
     o2 = lsx.chunked_attention(q, k, v, chunk, causal, checkpoint="inputs")
     o2.backward(d_o)
     assert torch.equal(o, o2)
-    for g, t in zip(got, (q, k, v)):
-        assert torch.equal(g, t.grad)  # same kernels on the same O, LSE
+    # same kernels on the same O, LSE: dK, dV identical; dQ's fp32 partial
+    # sums land in a varying order (lsx.set_deterministic), so it agrees to
+    # summation noise
+    assert rel_fro(f64(got[0]), f64(q.grad)) <= 1e-3
+    for g, t in zip(got[1:], (k, v)):
+        assert torch.equal(g, t.grad)

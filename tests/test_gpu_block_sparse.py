@@ -80,6 +80,16 @@ def test_full_mask_equals_dense_chunked_path():
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
         g1 = lsx.block_sparse_bwd(q, k, v, o1, l1, d_o, full, causal)
         g2 = lsx.chunked_bwd(q, k, v, o2, l2, d_o, 512, causal)
+        # dK, dV identical; dQ's fp32 partial sums land in a varying order
+        assert rel_fro(f64(g1[0]), f64(g2[0])) <= 1e-3
+        for a, b in zip(g1[1:], g2[1:]):
+            assert torch.equal(a, b)
+        lsx.set_deterministic(True)
+        try:
+            g1 = lsx.block_sparse_bwd(q, k, v, o1, l1, d_o, full, causal)
+            g2 = lsx.chunked_bwd(q, k, v, o2, l2, d_o, 512, causal)
+        finally:
+            lsx.set_deterministic(False)
         for a, b in zip(g1, g2):
             assert torch.equal(a, b)
 

@@ -44,10 +44,18 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=[False, True], ids=["fused_dq", "owner_dq"])
+def dq_mode(request):
+    """Runs a test in both backward reduction orders (lsx.set_deterministic)."""
+    lsx.set_deterministic(request.param)
+    yield request.param
+    lsx.set_deterministic(False)
+
+
 @pytest.mark.parametrize("case", CASES)
 @pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("copies", [True, False], ids=["operand_copies", "as_stored"])
-def test_chunk_bwd_matches_oracle(case, grad_dtype, copies):
+def test_chunk_bwd_matches_oracle(case, grad_dtype, copies, dq_mode):
     b, hq, hkv, lq, lk, d, q_off, kv_off, causal = case
     q, k, v, d_o = make(b, hq, hkv, lq, lk, d, seed=lq + 7 * lk)
     # the saved O and LSE come from the GPU forward (as in training)
@@ -60,7 +68,7 @@ def test_chunk_bwd_matches_oracle(case, grad_dtype, copies):
     check_grads(grads, ref)
 
 
-def test_chunked_bwd_over_chunk_pairs_accumulates():
+def test_chunked_bwd_over_chunk_pairs_accumulates(dq_mode):
     # two query chunks x two key chunks, causal, f32 accumulation across pairs
     n, c = 1024, 512
     q, k, v, d_o = make(1, 4, 4, n, n, 128, seed=3, amp=0.5)
@@ -82,13 +90,57 @@ def test_chunked_bwd_over_chunk_pairs_accumulates():
     check_grads(g2, ref)
 
 
-def test_backward_is_deterministic():
-    q, k, v, d_o = make(1, 4, 4, 768, 768, 128, seed=5)
+@pytest.mark.parametrize("d", [128, 64])
+def test_deterministic_mode_repeats_bit_for_bit(d):
+    q, k, v, d_o = make(1, 4, 4, 768, 768, d, seed=5)
     o, lse = lsx.chunk_fwd(q, k, v, 0, 0, True)
-    a = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
-    b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
+    lsx.set_deterministic(True)
+    try:
+        a = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
+        b = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True)
+    finally:
+        lsx.set_deterministic(False)
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
+def test_fused_dq_agrees_with_owner_dq(grad_dtype):
+    # The fused kernel runs the same dK / dV products in the same order as
+    # the dK/dV kernel (identical bytes).  Its dQ varies between calls only
+    # in the order the fp32 partial sums land (then one bf16 rounding), and
+    # differs from the owner kernel's dQ also where the two kernels' dS
+    # (LSE applied on the tensor cores vs per element) round to
+    # neighbouring bf16 values.
+    q, k, v, d_o = make(2, 4, 2, 900, 1100, 128, seed=21)
+    o, lse = lsx.chunk_fwd(q, k, v, 200, 0, True)
+    fused = lsx.chunk_bwd(q, k, v, o, lse, d_o, 200, 0, True, grad_dtype=grad_dtype)
+    again = lsx.chunk_bwd(q, k, v, o, lse, d_o, 200, 0, True, grad_dtype=grad_dtype)
+    lsx.set_deterministic(True)
+    try:
+        owner = lsx.chunk_bwd(q, k, v, o, lse, d_o, 200, 0, True, grad_dtype=grad_dtype)
+    finally:
+        lsx.set_deterministic(False)
+    torch.cuda.synchronize()
+    assert lsx.sync_status() == 0
+    for name, x, y, z in zip(("dQ", "dK", "dV"), fused, again, owner):
+        if name == "dQ":
+            assert rel_fro(f64(x), f64(z)) <= 2e-3
+            assert rel_fro(f64(x), f64(y)) <= 1e-3
+        else:
+            assert torch.equal(x, z) and torch.equal(x, y), name
+
+
+def test_fused_dq_adds_into_f32_dq():
+    # min workspace + f32 dq: the fused kernel adds straight into dq
+    q, k, v, d_o = make(1, 2, 2, 520, 640, 128, seed=33)
+    o, lse = lsx.chunk_fwd(q, k, v, 120, 0, True)
+    base = [torch.randn(t.shape, dtype=torch.float32, device=DEV) for t in (q, k, v)]
+    outs = [t.clone() for t in base]
+    lsx.chunk_bwd(q, k, v, o, lse, d_o, 120, 0, True, dq=outs[0], dk=outs[1], dv=outs[2],
+                  accumulate=True, use_copies=False)
+    ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), 120, 0, True)
+    check_grads([x - b for x, b in zip(outs, base)], ref)
 
 
 def test_operand_layouts_give_the_same_gradients():
