@@ -230,7 +230,7 @@ struct DkdvSmem {
   float lse2[2][128];             // LSE * log2(e); +inf for rows without keys
   float delta[2][128];
   uint64_t kv_full, kv_empty, final_bar, ones_full;
-  uint64_t st_full[2], st_empty[2];
+  uint64_t q_full[2], q_empty[2], o_full[2], o_empty[2];  // Q_i (+ statistics), dO_i slots
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_full, p_full, dkv_done;
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ only
@@ -338,8 +338,10 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.final_bar, 1);
     mbar_init(&sm.ones_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sm.st_full[s], 1);
-      mbar_init(&sm.st_empty[s], 1);
+      mbar_init(&sm.q_full[s], 1);
+      mbar_init(&sm.q_empty[s], 1);
+      mbar_init(&sm.o_full[s], 1);
+      mbar_init(&sm.o_empty[s], 1);
       mbar_init(&sm.lse_full[s], 32);
       mbar_init(&sm.lse_empty[s], 512);
     }
@@ -391,15 +393,21 @@ __global__ void __launch_bounds__(640, 1)
         for (int64_t s = 0; s < x.n_i; ++s) {
           int64_t h, i;
           dkdv_step(p, x, s, h, i);
-          // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV)
-          if (!mbar_wait(&sm.st_empty[qs], qph ^ 1, guard)) { ok = false; break; }
+          // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV);
+          // the two slots are freed separately (the fused form frees Q_i's
+          // first) and S^T waits only for Q_i
+          if (!mbar_wait(&sm.q_empty[qs], qph ^ 1, guard)) { ok = false; break; }
           if (lane == 0) {
-            mbar_arrive_expect_tx(&sm.st_full[qs], 2 * kTile + (kRS ? 128 * 16 : 0));
-            load_tile<D, false>(sm.q[qs], &tm_q, &sm.st_full[qs], i * 128, h, x.b);
-            load_tile<D, false>(sm.d_o[qs], &tm_do, &sm.st_full[qs], i * 128, h, x.b);
+            mbar_arrive_expect_tx(&sm.q_full[qs], kTile + (kRS ? 128 * 16 : 0));
+            load_tile<D, false>(sm.q[qs], &tm_q, &sm.q_full[qs], i * 128, h, x.b);
             if constexpr (kRS)
-              tma_load_4d(sm.rs[qs], &tm_rs, &sm.st_full[qs], 0, static_cast<int>(i * 128),
+              tma_load_4d(sm.rs[qs], &tm_rs, &sm.q_full[qs], 0, static_cast<int>(i * 128),
                           static_cast<int>(h), static_cast<int>(x.b));
+          }
+          if (!mbar_wait(&sm.o_empty[qs], qph ^ 1, guard)) { ok = false; break; }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.o_full[qs], kTile);
+            load_tile<D, false>(sm.d_o[qs], &tm_do, &sm.o_full[qs], i * 128, h, x.b);
           }
           if (++qs == kQoStages) { qs = 0; qph ^= 1; }
           if constexpr (kRS) continue;
@@ -445,7 +453,7 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
-          if (!mbar_wait(&sm.st_full[qs], qph, guard)) { ok = false; break; }
+          if (!mbar_wait(&sm.q_full[qs], qph, guard)) { ok = false; break; }
           tc_fence_after();
           const uint32_t q_addr = smem_addr(sm.q[qs]);
           const uint32_t o_addr = smem_addr(sm.d_o[qs]);
@@ -455,8 +463,9 @@ __global__ void __launch_bounds__(640, 1)
           if (kDq && dq_pending) {  // dP^T reuses the columns of the last dQ^T
             if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
             dr_phase ^= 1;
-            tc_fence_after();
           }
+          if (!mbar_wait(&sm.o_full[qs], qph, guard)) { ok = false; break; }
+          tc_fence_after();
           mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
           if constexpr (kRS) mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
           mma_commit(&sm.s_full);
@@ -503,7 +512,10 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
           mma_commit(&sm.dkv_done);
-          if constexpr (!kDq) mma_commit(&sm.st_empty[qs]);  // (kDq: the reducer frees it)
+          if constexpr (!kDq) {  // (kDq: the reducer frees them)
+            mma_commit(&sm.q_empty[qs]);
+            mma_commit(&sm.o_empty[qs]);
+          }
           if (++qs == kQoStages) { qs = 0; qph ^= 1; }
         }
         if (!ok) break;
@@ -531,24 +543,27 @@ __global__ void __launch_bounds__(640, 1)
           dkdv_step(p, x, s, h, i);
           if (!mbar_wait(&sm.stage_full, sf_phase, guard)) { ok = false; break; }
           sf_phase ^= 1;
+          // one bulk group per half: the Q_i slot (queries 0..63) is freed as
+          // soon as its group has been read, so that Q_{i+2} loads earlier
           for (int half = 0; half < 2; ++half) {
             const int64_t q0 = i * 128 + 64 * half;
             int64_t rows = p.Lq - q0;
-            if (rows <= 0) continue;
             if (rows > 64) rows = 64;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(half ? sm.d_o[slot] : sm.q[slot]);
             float* dst = p.dq_acc + x.b * p.acc_sb + h * p.acc_sh + q0 * p.acc_sn;
-            if (p.acc_sn == 128) {
+            if (rows > 0 && p.acc_sn == 128) {
               bulk_reduce_add_f32(dst, src, static_cast<uint32_t>(rows * 512));
             } else {
               for (int64_t rr = 0; rr < rows; ++rr)
                 bulk_reduce_add_f32(dst + rr * p.acc_sn, src + rr * 512, 512u);
             }
+            bulk_commit();
           }
-          bulk_commit();
-          bulk_wait_read();
           any = true;
-          mbar_arrive(&sm.st_empty[slot]);
+          bulk_wait_read_but1();
+          mbar_arrive(&sm.q_empty[slot]);
+          bulk_wait_read();
+          mbar_arrive(&sm.o_empty[slot]);
           if (++slot == kQoStages) slot = 0;
         }
         if (!ok) break;

@@ -339,6 +339,10 @@ LSX_DEV void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
 }
 LSX_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LSX_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// ... all but the most recent group have been read
+LSX_DEV void bulk_wait_read_but1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 LSX_DEV void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Per-warpgroup register budget changes (all 4 warps of a warpgroup execute
