@@ -26,6 +26,12 @@
 //    with bulk TMA reduce-adds and frees the slots for the next loads once
 //    the TMA unit has read them.  dK and dV stay owned by one CTA each; dQ's
 //    summation order varies between runs.
+//    With kDq and D = 64, TMEM has room to spare and shared memory too:
+//      dQ_i = dS K        (SS, both MN-major)     TMEM [320,384) / [448,512)
+//    alternating between the two free 64-column regions, with dS^T in its
+//    own double-buffered shared tile written before P^T is published; the
+//    grad warps read dQ_{i-1} back during step i and add it with 16-byte
+//    vector atomics (one query row per thread), so no product waits on it.
 //  * dq_kernel (the deterministic form of dQ), query-tile-major: a work item is one 128-row query tile; it
 //    walks every visible key tile:
 //      S  = Q K_j^T, dP = dO V_j^T (SS)                TMEM [0,128), [128,256)
@@ -233,9 +239,12 @@ struct DkdvSmem {
   uint64_t q_full[2], q_empty[2], o_full[2], o_empty[2];  // Q_i (+ statistics), dO_i slots
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_full, p_full, dkv_done;
-  uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ only
+  uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
+  uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
   uint32_t tmem_base;
   int abort;
+  // dS^T tiles of the D = 64 fused form (128-byte swizzle: 1024-aligned)
+  alignas(1024) __nv_bfloat16 ds[D == 64 ? 2 : 1][D == 64 ? 128 * 128 : 8];
 };
 
 struct DkdvItem {
@@ -323,7 +332,9 @@ __global__ void __launch_bounds__(640, 1)
                 const __grid_constant__ CUtensorMap tm_rs,
                 const __grid_constant__ CUtensorMap tm_ones, const BwdParams p) {
   using Sm = DkdvSmem<D>;
-  static_assert(!kDq || D == 128, "fused dQ: the dQ^T tile spans TMEM lanes 0..127");
+  static_assert(!kDq || D == 128 || D == 64, "fused dQ: d = 128 or 64");
+  constexpr bool kQ128 = kDq && D == 128;  // dQ^T in the dP^T columns, staged, bulk-reduced
+  constexpr bool kQ64 = kDq && D == 64;    // dQ in free columns, vector atomics
   constexpr int kTile = 128 * D * 2;
   constexpr int kQoStages = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -353,6 +364,10 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.dq_full, 1);
     mbar_init(&sm.dq_drained, 512);
     mbar_init(&sm.stage_full, 512);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.dq_done[b], 1);
+      mbar_init(&sm.dq_free[b], 512);
+    }
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -434,6 +449,8 @@ __global__ void __launch_bounds__(640, 1)
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T = K^T dS^T
+      constexpr uint32_t kIdQ64 = idesc_bf16_f32(128, 64, 1, 1);  // dQ = dS K (D = 64)
+      int64_t n_dq = 0;  // dQ products issued (D = 64)
       uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0, ds_phase = 0, dr_phase = 0;
       bool issued = false, dq_pending = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
@@ -460,7 +477,7 @@ __global__ void __launch_bounds__(640, 1)
           const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
           mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
           if constexpr (kRS) mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
-          if (kDq && dq_pending) {  // dP^T reuses the columns of the last dQ^T
+          if (kQ128 && dq_pending) {  // dP^T reuses the columns of the last dQ^T
             if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
             dr_phase ^= 1;
           }
@@ -474,7 +491,7 @@ __global__ void __launch_bounds__(640, 1)
           p_phase ^= 1;
           const uint32_t bq = q_addr, bo = o_addr;
           tc_fence_after();
-          if constexpr (kDq) {
+          if constexpr (kQ128) {
             const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
             const uint32_t acc0 = s > 0 ? 1u : 0u;
 #pragma unroll
@@ -501,6 +518,7 @@ __global__ void __launch_bounds__(640, 1)
             mma_commit(&sm.dq_full);
             dq_pending = true;
           } else {
+            // (kQ64 runs the same dV / dK products, then dQ below)
             const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
             const uint32_t acc0 = s > 0 ? 1u : 0u;
 #pragma unroll
@@ -510,9 +528,28 @@ __global__ void __launch_bounds__(640, 1)
               mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
                      acc);
             }
+            if constexpr (kQ64) {
+              // dQ_i = dS K_j: A = dS^T's [key][query] tile and B = K_j's
+              // [key][d] tile, both MN-major; into the region of dQ_{i-2},
+              // once the grad warps have read that
+              const int buf = static_cast<int>(n_dq & 1);
+              if (n_dq >= 2) {
+                if (!mbar_wait(&sm.dq_free[buf], static_cast<uint32_t>((n_dq - 2) >> 1) & 1u,
+                               guard)) { ok = false; break; }
+                tc_fence_after();
+              }
+              const uint64_t da0 = sdesc_sw128(smem_addr(sm.ds[buf]), 128 * 128, 1024);
+              const uint64_t kb0 = sdesc_sw128(k_addr, 128 * 128, 1024);
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tmem + (buf ? 448u : 320u), da0 + mnmajor_step(kk), kb0 + mnmajor_step(kk),
+                       kIdQ64, kk > 0 ? 1u : 0u);
+              mma_commit(&sm.dq_done[buf]);
+              ++n_dq;
+            }
           }
           mma_commit(&sm.dkv_done);
-          if constexpr (!kDq) {  // (kDq: the reducer frees them)
+          if constexpr (!kQ128) {  // (kQ128: the reducer frees them)
             mma_commit(&sm.q_empty[qs]);
             mma_commit(&sm.o_empty[qs]);
           }
@@ -525,7 +562,7 @@ __global__ void __launch_bounds__(640, 1)
         mma_commit(&sm.final_bar);
         drain_wait(&sm.final_bar, 0, p.wait_ns);
       }
-    } else if (kDq && warp == 2 && lane == 0) {
+    } else if (kQ128 && warp == 2 && lane == 0) {
       // ------------------------------------------ dQ reducer (fused form)
       // Step by step: wait for the grad warps' staged scale * dQ_i (fp32
       // rows of 128; queries 0..63 in the Q_i slot, 64..127 in the dO_i
@@ -583,6 +620,32 @@ __global__ void __launch_bounds__(640, 1)
     uint32_t d_count = 0;
     const float sl2 = p.scale_log2;
     const float2 sc2 = make_float2(sl2, sl2);
+    // D = 64 fused dQ: steps issued so far and the last step's (b, h, i);
+    // drain64(m, ...) reads dQ of step m (query row = this lane, 16 of its
+    // 64 columns), frees its TMEM region and adds scale * dQ into the
+    // accumulator with four 16-byte atomics
+    int64_t n_g = 0, pb = 0, ph = 0, pi = 0;
+    bool grad_ok = true;
+    auto drain64 = [&](int64_t m, int64_t b, int64_t h, int64_t i) -> bool {
+      const int buf = static_cast<int>(m & 1);
+      if (!mbar_wait(&sm.dq_done[buf], static_cast<uint32_t>(m >> 1) & 1u, guard)) return false;
+      tc_fence_after();
+      uint32_t w[16];
+      tmem_ld16_sync(tmem + lane_base + (buf ? 448u : 320u) + 16 * qtr, w);
+      tc_fence_before();
+      mbar_arrive(&sm.dq_free[buf]);
+      const int64_t qrow = i * 128 + row;
+      if (qrow < p.Lq) {
+        float* dst = p.dq_acc + b * p.acc_sb + h * p.acc_sh + qrow * p.acc_sn + 16 * qtr;
+        const float sc = p.scale;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4)
+          red_add_v4_f32(dst + 4 * c4, __uint_as_float(w[4 * c4]) * sc,
+                         __uint_as_float(w[4 * c4 + 1]) * sc, __uint_as_float(w[4 * c4 + 2]) * sc,
+                         __uint_as_float(w[4 * c4 + 3]) * sc);
+      }
+      return true;
+    };
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
@@ -648,11 +711,29 @@ __global__ void __launch_bounds__(640, 1)
           mbar_arrive(&sm.lse_empty[ls]);
           if (++ls == 2) { ls = 0; lph ^= 1; }
         }
+        if constexpr (kQ64) {
+          // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle)
+          // into its own tile; the dQ product that last read it (two steps
+          // back) completed before this warp's previous drain
+          uint8_t* line = reinterpret_cast<uint8_t*>(sm.ds[n_g & 1]) + (qtr >> 1) * 16384 + row * 128;
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int ch = (qtr & 1) * 4 + c4;
+            *reinterpret_cast<uint4*>(line + ((ch ^ (row & 7)) << 4)) =
+                make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
+          }
+          fence_proxy_async_smem();
+        }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full);
         ++d_count;
-        if constexpr (kDq) {
+        if constexpr (kQ64) {
+          if (n_g >= 1 && !drain64(n_g - 1, pb, ph, pi)) { ok = false; break; }
+          pb = x.b; ph = h; pi = i;
+          ++n_g;
+        }
+        if constexpr (kQ128) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle,
           // the layout a TMA load of such a tile produces) into the slot of
           // dO_i, once the dV product has finished reading it
@@ -700,10 +781,10 @@ __global__ void __launch_bounds__(640, 1)
           mbar_arrive(&sm.stage_full);
         }
       }
-      if (!ok) break;
+      if (!ok) { grad_ok = false; break; }
       // epilogue: half 0 writes dV, half 1 writes dK (times scale)
       if (x.n_i > 0) {
-        if (!mbar_wait(&sm.dkv_done, (d_count - 1) & 1, guard)) break;
+        if (!mbar_wait(&sm.dkv_done, (d_count - 1) & 1, guard)) { grad_ok = false; break; }
         tc_fence_after();
       }
       const int64_t krow = x.j * 128 + row;
@@ -733,6 +814,7 @@ __global__ void __launch_bounds__(640, 1)
       }
       tc_fence_before();
     }
+    if (kQ64 && grad_ok && n_g >= 1) drain64(n_g - 1, pb, ph, pi);  // the last dQ
   }
   tc_fence_before();
   __syncthreads();
@@ -1040,16 +1122,16 @@ __global__ void __launch_bounds__(640, 1)
   }
 }
 
-// dq (bf16 or f32 view, D = 128) = acc (dense fp32 [B*Hq*Lq][128]),
-// optionally added to what dq holds; four columns per thread.
+// dq (bf16 or f32 view) = acc (dense fp32 [B*Hq*Lq][D]), optionally added
+// to what dq holds; four columns per thread (c4 = D / 4 per row).
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc, void* dq,
                                                          int f32, int64_t sb, int64_t sh,
                                                          int64_t sn, int64_t Hq, int64_t Lq,
-                                                         int64_t total4, int accumulate) {
+                                                         int64_t total4, int c4, int accumulate) {
   for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total4;
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t rowi = t >> 5;
-    const int64_t col = (t & 31) * 4;
+    const int64_t rowi = t / c4;
+    const int64_t col = (t % c4) * 4;
     const int64_t n = rowi % Lq, bh = rowi / Lq;
     const int64_t off = (bh / Hq) * sb + (bh % Hq) * sh + n * sn + col;
     float4 a = reinterpret_cast<const float4*>(acc)[t];
@@ -1098,8 +1180,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                     cudaStream_t s, const BlockLists* bl) {
   // fused dK/dV/dQ: D = 128, not in deterministic mode, and somewhere to
   // add dQ into (the fp32 accumulator in the workspace, or an f32 dq)
-  const bool fused = D == 128 && !ctx.deterministic &&
-                     (cp.dq_acc != nullptr || dq.dtype == LSX_F32);
+  const bool fused = !ctx.deterministic && (cp.dq_acc != nullptr || dq.dtype == LSX_F32);
   const bool direct = fused && dq.dtype == LSX_F32;  // add straight into dq
   const bool tr = !fused && cp.kt != nullptr;
   const bool rs = cp.stats.rows != nullptr;
@@ -1146,7 +1227,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
 
   // dK, dV (and dQ): items (key tile, b, kv head)
   p.n_items = p.n_ktiles * q.B * k.H;
-  if constexpr (D == 128) if (fused) {
+  if (fused) {
     if (direct) {
       p.dq_acc = static_cast<float*>(dq.data);
       p.acc_sb = dq.stride_b; p.acc_sh = dq.stride_h; p.acc_sn = dq.stride_n;
@@ -1178,7 +1259,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
     timing_begin(kKidDqConvert, s);
     dq_convert_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
         cp.dq_acc, dq.data, dq.dtype == LSX_F32, dq.stride_b, dq.stride_h, dq.stride_n, q.H, q.N,
-        total4, accumulate);
+        total4, D / 4, accumulate);
     timing_end(kKidDqConvert, s);
     return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
   }
@@ -1223,10 +1304,8 @@ size_t stats_bytes(const lsx_tensor& q) {
 }
 size_t scratch_bytes(const lsx_tensor& q, const lsx_tensor& k) {
   size_t n = transposed_bytes(k);
-  if (q.D == 128) {
-    const size_t acc = static_cast<size_t>(q.B * q.H * q.N) * 128 * sizeof(float);
-    if (acc > n) n = acc;
-  }
+  const size_t acc = static_cast<size_t>(q.B * q.H * q.N * q.D) * sizeof(float);
+  if (acc > n) n = acc;
   return (n + 255) / 256 * 256;
 }
 }  // namespace
@@ -1243,7 +1322,7 @@ BwdCopies bwd_tc_copies(const lsx_tensor& q, const lsx_tensor& k, void* base) {
   c.stats.rows = st + 2 * 128 * 16;
   char* scratch = st + stats_bytes(q);
   c.kt = scratch;
-  if (q.D == 128) c.dq_acc = reinterpret_cast<float*>(scratch);
+  c.dq_acc = reinterpret_cast<float*>(scratch);
   return c;
 }
 

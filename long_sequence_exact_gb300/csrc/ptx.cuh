@@ -337,6 +337,13 @@ LSX_DEV void bulk_reduce_add_f32(float* dst, const void* src, uint32_t bytes) {
       "r"(smem_addr(src)), "r"(bytes)
       : "memory");
 }
+// Fire-and-forget add of four consecutive floats (16-byte aligned) in
+// global memory, performed at L2.
+LSX_DEV void red_add_v4_f32(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
 LSX_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LSX_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // ... all but the most recent group have been read
