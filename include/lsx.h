@@ -157,7 +157,7 @@ int attn_tree_merge(const lsx_tensor* o_parts, int64_t part_stride_o,
  * 16 bytes per query row of row statistics (-LSE/scale and -delta as bf16
  * triples), which the dK/dV products add to their score tiles on the tensor
  * cores instead of per element, and one scratch region used EITHER as the
- * fp32 dQ accumulator of the fused D = 128 kernel (4 bytes x B x Hq x Lq x
+ * fp32 dQ accumulator of the fused kernel (bf16 inputs; 4 bytes x B x Hq x Lq x
  * D; see lsx_set_deterministic) OR as a key-contiguous copy of K, which the
  * separate dQ kernel reads at the tensor cores' faster operand layout.
  * With less, the statistics are applied per element, K is read as stored,
@@ -320,7 +320,7 @@ const char* lsx_status_string(int code);
  * the default (10 s).  Process-wide; affects launches made after the call. */
 void lsx_set_wait_limit_ns(uint64_t ns);
 
-/* Backward reduction order.  on == 0 (the default): for D = 128 one kernel
+/* Backward reduction order.  on == 0 (the default): for bf16 inputs one kernel
  * computes dK, dV and dQ together and adds each key tile's contribution to
  * dQ into an fp32 accumulator with global atomic adds, so dQ's rounding
  * depends on the order in which those adds land (results agree with the

@@ -125,8 +125,8 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& lse, int accumulate, void* vt,
                   const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
-// tcgen05 tensor-core backward (bf16 inputs).  For D = 128 (unless the
-// deterministic mode is set) one kernel computes dK, dV and dQ, adding each
+// tcgen05 tensor-core backward (bf16 inputs).  Unless the deterministic
+// mode is set, one kernel computes dK, dV and dQ (D = 128 or 64), adding each
 // key tile's dQ contribution into an fp32 accumulator: copies.dq_acc
 // (dense [B, Hq, Lq, D], zeroed and converted to dq by the launcher) or,
 // when dq itself is f32, dq directly.  Otherwise two kernels own their
