@@ -155,3 +155,41 @@ def test_operand_layouts_give_the_same_gradients():
                       use_copies=False)
     for x, y in zip(a, b):
         assert rel_fro(f64(x), f64(y)) <= 2e-3
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_fused_dq_accumulates_into_bf16_dq(d):
+    # full workspace + bf16 dq: fp32 accumulator, then the conversion kernel
+    # adds it to what dq holds
+    q, k, v, d_o = make(2, 4, 2, 300, 420, d, seed=41)
+    o, lse = lsx.chunk_fwd(q, k, v, 100, 0, True)
+    base = [torch.randn(t.shape, device=DEV).to(torch.bfloat16) for t in (q, k, v)]
+    outs = [t.clone() for t in base]
+    lsx.chunk_bwd(q, k, v, o, lse, d_o, 100, 0, True, dq=outs[0], dk=outs[1], dv=outs[2],
+                  accumulate=True)
+    torch.cuda.synchronize()
+    assert lsx.sync_status() == 0
+    ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), 100, 0, True)
+    # the bf16 outputs round (base + gradient): compare against the oracle sum
+    for name, x, b, r in zip(("dQ", "dK", "dV"), outs, base, ref):
+        e = rel_fro(f64(x), f64(b) + r)
+        assert e <= 1e-2, f"{name}: {e:.3e}"
+
+
+@pytest.mark.parametrize("d", [128, 64])
+def test_fused_dq_into_strided_f32_view(d):
+    # dq as a [B, N, H, D] buffer viewed as [B, H, N, D]: rows are H*D apart,
+    # so the fused kernel adds row by row (per-row bulk adds at d = 128,
+    # strided vector adds at d = 64)
+    b, h, n = 1, 3, 333
+    q, k, v, d_o = make(b, h, h, n, n, d, seed=43)
+    o, lse = lsx.chunk_fwd(q, k, v, 0, 0, True)
+    dq = torch.zeros((b, n, h, d), dtype=torch.float32, device=DEV).permute(0, 2, 1, 3)
+    for copies in (True, False):
+        dq.zero_()
+        _, dk, dv = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True, dq=dq,
+                                  grad_dtype=torch.float32, use_copies=copies)
+        torch.cuda.synchronize()
+        assert lsx.sync_status() == 0
+        ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), 0, 0, True)
+        check_grads((dq, dk, dv), ref)
