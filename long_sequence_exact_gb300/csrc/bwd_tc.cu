@@ -1181,7 +1181,10 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   // fused dK/dV/dQ: D = 128, not in deterministic mode, and somewhere to
   // add dQ into (the fp32 accumulator in the workspace, or an f32 dq)
   const bool fused = !ctx.deterministic && (cp.dq_acc != nullptr || dq.dtype == LSX_F32);
-  const bool direct = fused && dq.dtype == LSX_F32;  // add straight into dq
+  // add straight into an f32 dq when its rows are contiguous (one bulk add
+  // per half tile) or when there is no accumulator; a strided dq with the
+  // workspace goes through the accumulator (row-by-row adds are 2x slower)
+  const bool direct = fused && dq.dtype == LSX_F32 && (dq.stride_n == D || cp.dq_acc == nullptr);
   const bool tr = !fused && cp.kt != nullptr;
   const bool rs = cp.stats.rows != nullptr;
   CUtensorMap tq, tk, tv, tdo, tkt, trs, tones;
