@@ -90,10 +90,17 @@ struct BwdParams {
   const int32_t* row_list;  // stride n_ktiles
   const int32_t* col_count;
   const int32_t* col_list;  // stride n_qtiles
-  // fused dQ: fp32 accumulator and its strides (elements)
+  // fused dQ: fp32 accumulator and its strides (elements); with acc_tma
+  // (D = 128) the accumulator is transposed, [B][Hq][128][Np], and is added
+  // into through the tensor map tm_acc
   float* dq_acc;
   int64_t acc_sb, acc_sh, acc_sn;
+  int acc_tma;
 };
+
+// Row pitch (elements) of the transposed fp32 dQ accumulator [.][128][Np]:
+// N rounded up to 16-byte rows, as tensor maps require.
+__host__ __device__ inline int64_t dq_acc_pitch(int64_t n) { return (n + 3) / 4 * 4; }
 
 // TMEM column (relative to the 128-column fp32 tile) of the packed bf16
 // operand for K step kk (16 elements = 8 packed columns).
@@ -330,7 +337,8 @@ __global__ void __launch_bounds__(640, 1)
                 const __grid_constant__ CUtensorMap tm_v,
                 const __grid_constant__ CUtensorMap tm_do,
                 const __grid_constant__ CUtensorMap tm_rs,
-                const __grid_constant__ CUtensorMap tm_ones, const BwdParams p) {
+                const __grid_constant__ CUtensorMap tm_ones,
+                const __grid_constant__ CUtensorMap tm_acc, const BwdParams p) {
   using Sm = DkdvSmem<D>;
   static_assert(!kDq || D == 128 || D == 64, "fused dQ: d = 128 or 64");
   constexpr bool kQ128 = kDq && D == 128;  // dQ^T in the dP^T columns, staged, bulk-reduced
@@ -588,7 +596,13 @@ __global__ void __launch_bounds__(640, 1)
             if (rows > 64) rows = 64;
             const uint8_t* src = reinterpret_cast<const uint8_t*>(half ? sm.d_o[slot] : sm.q[slot]);
             float* dst = p.dq_acc + x.b * p.acc_sb + h * p.acc_sh + q0 * p.acc_sn;
-            if (rows > 0 && p.acc_sn == 128) {
+            if (p.acc_tma) {
+              // two boxes of [128 d][32 queries] (transposed accumulator)
+              for (int bx = 0; bx < 2; ++bx)
+                if (q0 + 32 * bx < p.Lq)
+                  tma_reduce_add_4d(&tm_acc, src + bx * 16384, static_cast<int>(q0 + 32 * bx), 0,
+                                    static_cast<int>(h), static_cast<int>(x.b));
+            } else if (rows > 0 && p.acc_sn == 128) {
               bulk_reduce_add_f32(dst, src, static_cast<uint32_t>(rows * 512));
             } else {
               for (int64_t rr = 0; rr < rows; ++rr)
@@ -768,10 +782,24 @@ __global__ void __launch_bounds__(640, 1)
           tmem_ld_wait32(u);
           tc_fence_before();
           mbar_arrive(&sm.dq_drained);
-          // stage scale * dQ^T as [query][d] fp32 rows of 512 bytes: the
-          // dQ^T MMA (complete) was the last reader of both slots; each warp
-          // store covers 128 consecutive bytes of one row
-          {
+          // stage scale * dQ^T (queries 0..63 in the Q_i slot, 64..127 in
+          // the dO_i slot; the dQ^T MMA, complete, was the last reader of
+          // both): as [query][d] fp32 rows of 512 bytes (each warp store
+          // covers 128 consecutive bytes of one row) or, for the transposed
+          // accumulator, as swizzled [d][32 queries] boxes
+          if (p.acc_tma) {
+            // transposed accumulator: this quarter's 32 queries are box
+            // (qtr & 1) of the slot, [128 d][32 queries] with the 128-byte
+            // swizzle; eight 16-byte stores per thread, conflict-free
+            uint8_t* sb = reinterpret_cast<uint8_t*>(qtr < 2 ? sm.q[gs_prev] : sm.d_o[gs_prev]) +
+                          (qtr & 1) * 16384 + row * 128;
+            const float sc = p.scale;
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<float4*>(sb + ((c ^ (row & 7)) << 4)) =
+                  make_float4(__uint_as_float(u[4 * c]) * sc, __uint_as_float(u[4 * c + 1]) * sc,
+                              __uint_as_float(u[4 * c + 2]) * sc, __uint_as_float(u[4 * c + 3]) * sc);
+          } else {
             float* stage = reinterpret_cast<float*>(qtr < 2 ? sm.q[gs_prev] : sm.d_o[gs_prev]) +
                            (qtr & 1) * 32 * 128 + row;
 #pragma unroll
@@ -1156,6 +1184,50 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict
   }
 }
 
+// dq (bf16 or f32 view, D = 128) = the transposed accumulator
+// [B*Hq][128][Np], optionally added to what dq holds.  A block moves 32
+// queries x 128 dims through shared memory: reads along queries, writes
+// along d (four columns per thread).
+__global__ void __launch_bounds__(256) dq_convert_t_kernel(const float* __restrict__ acc, void* dq,
+                                                           int f32, int64_t sb, int64_t sh,
+                                                           int64_t sn, int64_t Hq, int64_t Lq,
+                                                           int64_t np, int accumulate) {
+  __shared__ float tile[128][33];
+  const int64_t bh = blockIdx.y;
+  const int64_t q0 = static_cast<int64_t>(blockIdx.x) * 32;
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const float* src = acc + bh * 128 * np;
+  for (int d = w; d < 128; d += 8)
+    tile[d][lane] = (q0 + lane < Lq) ? src[d * np + q0 + lane] : 0.f;
+  __syncthreads();
+  const int64_t b = bh / Hq, h = bh % Hq;
+  for (int qq = w; qq < 32; qq += 8) {
+    const int64_t q = q0 + qq;
+    if (q >= Lq) break;
+    float4 a = make_float4(tile[4 * lane][qq], tile[4 * lane + 1][qq], tile[4 * lane + 2][qq],
+                           tile[4 * lane + 3][qq]);
+    const int64_t off = b * sb + h * sh + q * sn + 4 * lane;
+    if (f32) {
+      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dq) + off);
+      if (accumulate) {
+        const float4 o = *d;
+        a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+      }
+      *d = a;
+    } else {
+      uint2* d = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dq) + off);
+      if (accumulate) {
+        const uint2 o = *d;
+        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&o.x);
+        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&o.y);
+        a.x += __low2float(lo); a.y += __high2float(lo);
+        a.z += __low2float(hi); a.w += __high2float(hi);
+      }
+      *d = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
+    }
+  }
+}
+
 bool map_rows(CUtensorMap* m, const lsx_tensor& t) {
   return make_map_bf16_4d(m, t.data, t.B, t.H, t.N, t.D, t.stride_b, t.stride_h, t.stride_n,
                           128);
@@ -1230,6 +1302,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
 
   // dK, dV (and dQ): items (key tile, b, kv head)
   p.n_items = p.n_ktiles * q.B * k.H;
+  CUtensorMap tacc = tk;  // (unused unless p.acc_tma)
+  p.acc_tma = 0;
   if (fused) {
     if (direct) {
       p.dq_acc = static_cast<float*>(dq.data);
@@ -1238,6 +1312,17 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
         const int rc = launch_zero(dq, ctx, s);
         if (rc != LSX_OK) return rc;
       }
+    } else if (D == 128) {
+      // transposed accumulator [B][Hq][128][Np], added into by tensor-map
+      // reduce-adds of [128 d][32 queries] boxes
+      const int64_t np = dq_acc_pitch(q.N);
+      p.dq_acc = cp.dq_acc;
+      p.acc_tma = 1;
+      p.acc_sn = 1; p.acc_sh = 128 * np; p.acc_sb = q.H * 128 * np;
+      if (!make_map_f32_rows32(&tacc, cp.dq_acc, q.B, q.H, 128, q.N, np)) return LSX_ERR_LAUNCH;
+      if (cudaMemsetAsync(cp.dq_acc, 0, static_cast<size_t>(q.B * q.H * 128 * np) * sizeof(float),
+                          s) != cudaSuccess)
+        return LSX_ERR_LAUNCH;
     } else {
       p.dq_acc = cp.dq_acc;
       p.acc_sn = D; p.acc_sh = q.N * D; p.acc_sb = q.H * q.N * D;
@@ -1252,10 +1337,19 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidBwdFused, s);
-    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, p);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, tacc, p);
     timing_end(kKidBwdFused, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
     if (direct) return LSX_OK;
+    if (p.acc_tma) {
+      timing_begin(kKidDqConvert, s);
+      const dim3 cgrid(static_cast<unsigned>(ceil_div(q.N, 32)), static_cast<unsigned>(q.B * q.H));
+      dq_convert_t_kernel<<<cgrid, 256, 0, s>>>(cp.dq_acc, dq.data, dq.dtype == LSX_F32,
+                                                dq.stride_b, dq.stride_h, dq.stride_n, q.H, q.N,
+                                                dq_acc_pitch(q.N), accumulate);
+      timing_end(kKidDqConvert, s);
+      return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+    }
     const int64_t total4 = q.B * q.H * q.N * (D / 4);
     int64_t blocks = (total4 + 255) / 256;
     if (blocks > 8 * ctx.sm_count) blocks = 8 * ctx.sm_count;
@@ -1274,7 +1368,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
     timing_begin(kKidDkdv, s);
-    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, p);
+    kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, tk, p);
     timing_end(kKidDkdv, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
   }
@@ -1307,7 +1401,9 @@ size_t stats_bytes(const lsx_tensor& q) {
 }
 size_t scratch_bytes(const lsx_tensor& q, const lsx_tensor& k) {
   size_t n = transposed_bytes(k);
-  const size_t acc = static_cast<size_t>(q.B * q.H * q.N * q.D) * sizeof(float);
+  // the D = 128 accumulator is transposed with rows padded to dq_acc_pitch
+  const int64_t rows = q.D == 128 ? dq_acc_pitch(q.N) : q.N;
+  const size_t acc = static_cast<size_t>(q.B * q.H * rows * q.D) * sizeof(float);
   if (acc > n) n = acc;
   return (n + 255) / 256 * 256;
 }

@@ -344,6 +344,18 @@ LSX_DEV void red_add_v4_f32(float* p, float a, float b, float c, float d) {
                "f"(c), "f"(d)
                : "memory");
 }
+// Bulk asynchronous reduce-add of one 4-D box from shared memory into the
+// tensor `map` describes (element type and swizzle from the map; elements
+// outside the tensor are skipped).  c0 * element size is a multiple of 16
+// bytes at every call site, and no coordinate is negative.
+LSX_DEV void tma_reduce_add_4d(const CUtensorMap* map, const void* src, int c0, int c1, int c2,
+                               int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group "
+      "[%0, {%2, %3, %4, %5}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_addr(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
 LSX_DEV void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 LSX_DEV void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // ... all but the most recent group have been read

@@ -74,4 +74,25 @@ inline bool make_map_bf16_rows8(CUtensorMap* map, const void* base, int64_t B,
   return r == CUDA_SUCCESS;
 }
 
+// Tiled map over a dense fp32 array [B][H][R][Np] (Np = row pitch in
+// elements, a multiple of 4; the first N elements of each row are the
+// tensor), box {32, R, 1, 1} with the 128-byte swizzle: one box is R rows of
+// 32 floats.  Used as the destination of bulk reduce-adds; elements past N
+// are not touched.  Returns false when the driver rejects the map.
+inline bool make_map_f32_rows32(CUtensorMap* map, const void* base, int64_t B, int64_t H,
+                                int64_t R, int64_t N, int64_t Np) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)N, (cuuint64_t)R, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(Np * 4), (cuuint64_t)(R * Np * 4),
+                           (cuuint64_t)(H * R * Np * 4)};
+  cuuint32_t box[4] = {32u, (cuuint32_t)R, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace lsx
