@@ -8,7 +8,7 @@ batch row at a time to bound the float32 scratch.  The same call on the same
 device type returns the same values, so the oracle (on the host) and the
 CUDA path see identical inputs.
 
-Workloads (sizes of the pages' long-sequence settings, stated in the design doc):
+Workloads (the sizes of the long-sequence settings the methods are measured on):
   tiny_fp32_causal         fp32 causal, B=1 H=2 N=256 d=64, chunks of 64
   causal_32k_ring          bf16 causal, B=1 H=32 N=32768 d=128, chunks of 4096
   causal_128k_balanced     bf16 causal, B=1 H=32 N=131072 d=128, chunks of 4096
