@@ -193,3 +193,18 @@ def test_fused_dq_into_strided_f32_view(d):
         assert lsx.sync_status() == 0
         ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), 0, 0, True)
         check_grads((dq, dk, dv), ref)
+
+
+@pytest.mark.parametrize("d", [128, 64])
+@pytest.mark.parametrize("lq", [1, 7, 31])
+def test_short_query_chunks(d, lq, dq_mode):
+    # query chunks shorter than one 32-query reduce box: the accumulator
+    # boxes are mostly past the end of the sequence and must be clipped
+    q, k, v, d_o = make(1, 2, 1, lq, 50, d, seed=lq + d)
+    for causal, q_off in ((False, 0), (True, 49)):
+        o, lse = lsx.chunk_fwd(q, k, v, q_off, 0, causal)
+        grads = lsx.chunk_bwd(q, k, v, o, lse, d_o, q_off, 0, causal, grad_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert lsx.sync_status() == 0
+        ref = A.attn_bwd(f64(q), f64(k), f64(v), f64(d_o), q_off, 0, causal)
+        check_grads(grads, ref)
