@@ -90,9 +90,10 @@ struct BwdParams {
   const int32_t* row_list;  // stride n_ktiles
   const int32_t* col_count;
   const int32_t* col_list;  // stride n_qtiles
-  // fused dQ: fp32 accumulator and its strides (elements); with acc_tma
-  // (D = 128) the accumulator is transposed, [B][Hq][128][Np], and is added
-  // into through the tensor map tm_acc
+  // fused dQ: fp32 accumulator and its strides (elements); with acc_tma it
+  // is added into through the tensor map tm_acc: at D = 128 the accumulator
+  // is transposed, [B][Hq][128][Np]; at D = 64 it is [B][Hq][N][64] with the
+  // strides above (boxes of [128 queries][32 d])
   float* dq_acc;
   int64_t acc_sb, acc_sh, acc_sn;
   int acc_tma;
@@ -248,6 +249,7 @@ struct DkdvSmem {
   uint64_t s_full, p_full, dkv_done;
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
   uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
+  uint64_t stage_free[2];  // D = 64 with acc_tma: the dS^T tile's staged dQ has been read
   uint32_t tmem_base;
   int abort;
   // dS^T tiles of the D = 64 fused form (128-byte swizzle: 1024-aligned)
@@ -342,7 +344,7 @@ __global__ void __launch_bounds__(640, 1)
   using Sm = DkdvSmem<D>;
   static_assert(!kDq || D == 128 || D == 64, "fused dQ: d = 128 or 64");
   constexpr bool kQ128 = kDq && D == 128;  // dQ^T in the dP^T columns, staged, bulk-reduced
-  constexpr bool kQ64 = kDq && D == 64;    // dQ in free columns, vector atomics
+  constexpr bool kQ64 = kDq && D == 64;    // dQ in free columns, staged in the spent dS^T tile
   constexpr int kTile = 128 * D * 2;
   constexpr int kQoStages = 2;
   extern __shared__ uint8_t smem_raw[];
@@ -375,6 +377,7 @@ __global__ void __launch_bounds__(640, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&sm.dq_done[b], 1);
       mbar_init(&sm.dq_free[b], 512);
+      mbar_init(&sm.stage_free[b], 1);
     }
     fence_barrier_init();
   }
@@ -478,23 +481,27 @@ __global__ void __launch_bounds__(640, 1)
         tc_fence_after();
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
-          if (!mbar_wait(&sm.q_full[qs], qph, guard)) { ok = false; break; }
-          tc_fence_after();
           const uint32_t q_addr = smem_addr(sm.q[qs]);
           const uint32_t o_addr = smem_addr(sm.d_o[qs]);
-          const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
-          mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
-          if constexpr (kRS) mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
-          if (kQ128 && dq_pending) {  // dP^T reuses the columns of the last dQ^T
-            if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
-            dr_phase ^= 1;
+          // (kQ64: the S^T / dP^T of steps after an item's first were issued
+          // by the step before, ahead of its dQ)
+          if (!(kQ64 && s > 0)) {
+            if (!mbar_wait(&sm.q_full[qs], qph, guard)) { ok = false; break; }
+            tc_fence_after();
+            const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
+            mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
+            if constexpr (kRS) mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
+            if (kQ128 && dq_pending) {  // dP^T reuses the columns of the last dQ^T
+              if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
+              dr_phase ^= 1;
+            }
+            if (!mbar_wait(&sm.o_full[qs], qph, guard)) { ok = false; break; }
+            tc_fence_after();
+            mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
+            if constexpr (kRS) mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
+            mma_commit(&sm.s_full);
+            issued = true;
           }
-          if (!mbar_wait(&sm.o_full[qs], qph, guard)) { ok = false; break; }
-          tc_fence_after();
-          mma_rows_by_rows<D>(tmem + 128, v_addr, o_addr, kIdS);
-          if constexpr (kRS) mma_ss(tmem + 128, sel_d, st, kIdS, 1u);
-          mma_commit(&sm.s_full);
-          issued = true;
           if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
           p_phase ^= 1;
           const uint32_t bq = q_addr, bo = o_addr;
@@ -537,6 +544,27 @@ __global__ void __launch_bounds__(640, 1)
                      acc);
             }
             if constexpr (kQ64) {
+              // Q_i and dO_i have been read for the last time (dK, dV)
+              mma_commit(&sm.q_empty[qs]);
+              mma_commit(&sm.o_empty[qs]);
+              // The next step's S^T and dP^T go ahead of this step's dQ: the
+              // last readers of their columns (P^T by dV, dS^T by dK) precede
+              // them in issue order, and dQ reads only dS^T's shared tile and
+              // K_j, so dQ runs while the grad warps work on the next scores.
+              if (s + 1 < x.n_i) {
+                const uint32_t ns = qs + 1 == kQoStages ? 0u : qs + 1;
+                const uint32_t nph = qs + 1 == kQoStages ? qph ^ 1u : qph;
+                if (!mbar_wait(&sm.q_full[ns], nph, guard)) { ok = false; break; }
+                tc_fence_after();
+                const uint64_t nst = sdesc_interleave(smem_addr(sm.rs[ns]), 0, 128);
+                mma_rows_by_rows<D>(tmem + 0, k_addr, smem_addr(sm.q[ns]), kIdS);
+                if constexpr (kRS) mma_ss(tmem + 0, sel_c, nst, kIdS, 1u);
+                if (!mbar_wait(&sm.o_full[ns], nph, guard)) { ok = false; break; }
+                tc_fence_after();
+                mma_rows_by_rows<D>(tmem + 128, v_addr, smem_addr(sm.d_o[ns]), kIdS);
+                if constexpr (kRS) mma_ss(tmem + 128, sel_d, nst, kIdS, 1u);
+                mma_commit(&sm.s_full);
+              }
               // dQ_i = dS K_j: A = dS^T's [key][query] tile and B = K_j's
               // [key][d] tile, both MN-major; into the region of dQ_{i-2},
               // once the grad warps have read that
@@ -557,7 +585,7 @@ __global__ void __launch_bounds__(640, 1)
             }
           }
           mma_commit(&sm.dkv_done);
-          if constexpr (!kQ128) {  // (kQ128: the reducer frees them)
+          if constexpr (!kQ128 && !kQ64) {  // (kQ128: the reducer frees them; kQ64: above)
             mma_commit(&sm.q_empty[qs]);
             mma_commit(&sm.o_empty[qs]);
           }
@@ -570,6 +598,36 @@ __global__ void __launch_bounds__(640, 1)
         mma_commit(&sm.final_bar);
         drain_wait(&sm.final_bar, 0, p.wait_ns);
       }
+    } else if (kQ64 && p.acc_tma && warp == 2 && lane == 0) {
+      // ------------------------------------- dQ reducer (fused form, D = 64)
+      // Step m: wait for the grad warps' staged scale * dQ_m (fp32, two
+      // [128 queries][32 d] boxes with the 128-byte swizzle, in the dS^T
+      // tile that dQ_m's product has finished reading), add it into the
+      // target with two tensor-map reduce-adds, and free the tile for the
+      // dS^T of step m + 2 once the TMA unit has read it.
+      uint32_t sf_phase = 0;
+      int64_t m = 0;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DkdvItem x = dkdv_item(p, it);
+        bool ok = true;
+        for (int64_t s = 0; s < x.n_i; ++s, ++m) {
+          int64_t h, i;
+          dkdv_step(p, x, s, h, i);
+          if (!mbar_wait(&sm.stage_full, sf_phase, guard)) { ok = false; break; }
+          sf_phase ^= 1;
+          const uint8_t* src = reinterpret_cast<const uint8_t*>(sm.ds[kQ64 ? (m & 1) : 0]);
+          for (int bx = 0; bx < 2; ++bx)
+            tma_reduce_add_4d(&tm_acc, src + bx * 16384, 32 * bx, static_cast<int>(i * 128),
+                              static_cast<int>(h), static_cast<int>(x.b));
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(&sm.stage_free[m & 1]);
+        }
+        if (!ok) break;
+      }
+      bulk_wait_all();
     } else if (kQ128 && warp == 2 && lane == 0) {
       // ------------------------------------------ dQ reducer (fused form)
       // Step by step: wait for the grad warps' staged scale * dQ_i (fp32
@@ -636,8 +694,11 @@ __global__ void __launch_bounds__(640, 1)
     const float2 sc2 = make_float2(sl2, sl2);
     // D = 64 fused dQ: steps issued so far and the last step's (b, h, i);
     // drain64(m, ...) reads dQ of step m (query row = this lane, 16 of its
-    // 64 columns), frees its TMEM region and adds scale * dQ into the
-    // accumulator with four 16-byte atomics
+    // 64 columns) and frees its TMEM region.  With acc_tma it stages
+    // scale * dQ in step m's dS^T tile (which dQ_m's product has finished
+    // reading; the next dS^T written there, step m + 2's, waits for the
+    // reducer) for the reducer's tensor-map reduce-adds; otherwise it adds
+    // scale * dQ into the target with four 16-byte atomics.
     int64_t n_g = 0, pb = 0, ph = 0, pi = 0;
     bool grad_ok = true;
     auto drain64 = [&](int64_t m, int64_t b, int64_t h, int64_t i) -> bool {
@@ -648,6 +709,24 @@ __global__ void __launch_bounds__(640, 1)
       tmem_ld16_sync(tmem + lane_base + (buf ? 448u : 320u) + 16 * qtr, w);
       tc_fence_before();
       mbar_arrive(&sm.dq_free[buf]);
+      if (p.acc_tma) {
+        // box (qtr >> 1) holds d columns [32 (qtr >> 1), +32) as [128
+        // queries][32 floats], 128-byte swizzle; four 16-byte stores per
+        // thread, conflict-free.  Rows past Lq are clipped by the map.
+        const float sc = p.scale;
+        uint8_t* line =
+            reinterpret_cast<uint8_t*>(sm.ds[kQ64 ? buf : 0]) + (qtr >> 1) * 16384 + row * 128;
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const int ch = (qtr & 1) * 4 + c4;  // 16-byte chunk (4 d columns) in the line
+          *reinterpret_cast<float4*>(line + ((ch ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(w[4 * c4]) * sc, __uint_as_float(w[4 * c4 + 1]) * sc,
+                          __uint_as_float(w[4 * c4 + 2]) * sc, __uint_as_float(w[4 * c4 + 3]) * sc);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&sm.stage_full);
+        return true;
+      }
       const int64_t qrow = i * 128 + row;
       if (qrow < p.Lq) {
         float* dst = p.dq_acc + b * p.acc_sb + h * p.acc_sh + qrow * p.acc_sn + 16 * qtr;
@@ -671,6 +750,13 @@ __global__ void __launch_bounds__(640, 1)
         dkdv_step(p, x, s, h, i);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
+        if constexpr (kQ64) {
+          // this step's dS^T tile held the staged dQ of two steps back: the
+          // reducer has read it
+          if (p.acc_tma && n_g >= 2 &&
+              !mbar_wait(&sm.stage_free[n_g & 1], static_cast<uint32_t>((n_g - 2) >> 1) & 1u,
+                         guard)) { ok = false; break; }
+        }
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
         tc_fence_after();
         uint32_t us[32], ud[32];
@@ -728,7 +814,8 @@ __global__ void __launch_bounds__(640, 1)
         if constexpr (kQ64) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle)
           // into its own tile; the dQ product that last read it (two steps
-          // back) completed before this warp's previous drain
+          // back) completed before this warp's previous drain, and with
+          // acc_tma the reducer has read the dQ staged there since
           uint8_t* line = reinterpret_cast<uint8_t*>(sm.ds[n_g & 1]) + (qtr >> 1) * 16384 + row * 128;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
@@ -1330,6 +1417,11 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                           s) != cudaSuccess)
         return LSX_ERR_LAUNCH;
     }
+    // D = 64: staged [128 queries][32 d] boxes added through a tensor map
+    // when the target allows one (else 16-byte atomics from registers)
+    if (D == 64 && make_map_f32_box32x128(&tacc, p.dq_acc, q.B, q.H, q.N, D, p.acc_sb, p.acc_sh,
+                                          p.acc_sn))
+      p.acc_tma = 1;
     const size_t smem = sizeof(DkdvSmem<D>) + 1024;
     auto kern = rs ? dkdv_kernel<D, true, true> : dkdv_kernel<D, false, true>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1341,7 +1433,7 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
     timing_end(kKidBwdFused, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
     if (direct) return LSX_OK;
-    if (p.acc_tma) {
+    if (D == 128) {
       timing_begin(kKidDqConvert, s);
       const dim3 cgrid(static_cast<unsigned>(ceil_div(q.N, 32)), static_cast<unsigned>(q.B * q.H));
       dq_convert_t_kernel<<<cgrid, 256, 0, s>>>(cp.dq_acc, dq.data, dq.dtype == LSX_F32,

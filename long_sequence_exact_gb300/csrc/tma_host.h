@@ -95,4 +95,30 @@ inline bool make_map_f32_rows32(CUtensorMap* map, const void* base, int64_t B, i
   return r == CUDA_SUCCESS;
 }
 
+// Tiled map over an fp32 tensor with dims (innermost first) {D, N, H, B} and
+// element strides {1, sn, sh, sb}, box {32, 128, 1, 1} with the 128-byte
+// swizzle: one box is 128 rows of 32 floats.  Used as the destination of
+// tensor-map reduce-adds; rows past N are not touched.  Returns false when
+// the base is not 16-byte aligned, a stride is not a multiple of 16 bytes or
+// the driver rejects the map (the caller then adds another way).
+inline bool make_map_f32_box32x128(CUtensorMap* map, const void* base, int64_t B, int64_t H,
+                                   int64_t N, int64_t D, int64_t sb, int64_t sh, int64_t sn) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || B <= 0 || H <= 0 || N <= 0 || D < 32) return false;
+  if (H == 1) sh = N * sn;  // strides of extent-1 dimensions are never used
+  if (B == 1) sb = H * sh;
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) != 0 || sn <= 0 || sh <= 0 || sb <= 0 ||
+      (sn * 4) % 16 != 0 || (sh * 4) % 16 != 0 || (sb * 4) % 16 != 0)
+    return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)(sn * 4), (cuuint64_t)(sh * 4), (cuuint64_t)(sb * 4)};
+  cuuint32_t box[4] = {32u, 128u, 1u, 1u};
+  cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace lsx
