@@ -750,13 +750,6 @@ __global__ void __launch_bounds__(640, 1)
         dkdv_step(p, x, s, h, i);
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
-        if constexpr (kQ64) {
-          // this step's dS^T tile held the staged dQ of two steps back: the
-          // reducer has read it
-          if (p.acc_tma && n_g >= 2 &&
-              !mbar_wait(&sm.stage_free[n_g & 1], static_cast<uint32_t>((n_g - 2) >> 1) & 1u,
-                         guard)) { ok = false; break; }
-        }
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
         tc_fence_after();
         uint32_t us[32], ud[32];
@@ -814,8 +807,12 @@ __global__ void __launch_bounds__(640, 1)
         if constexpr (kQ64) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle)
           // into its own tile; the dQ product that last read it (two steps
-          // back) completed before this warp's previous drain, and with
-          // acc_tma the reducer has read the dQ staged there since
+          // back) completed before this warp's previous drain.  With acc_tma
+          // the tile has held that step's staged dQ since: wait (as late as
+          // possible) until the reducer has read it.
+          if (p.acc_tma && n_g >= 2 &&
+              !mbar_wait(&sm.stage_free[n_g & 1], static_cast<uint32_t>((n_g - 2) >> 1) & 1u,
+                         guard)) { tmem_st_wait(); ok = false; break; }
           uint8_t* line = reinterpret_cast<uint8_t*>(sm.ds[n_g & 1]) + (qtr >> 1) * 16384 + row * 128;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
