@@ -36,6 +36,7 @@ if ROOT not in sys.path:
 METRIC = "causal bf16 attn fwd+bwd TFLOP/s at 128K tokens, % of tensor peak"
 UNIT = "TFLOP/s"
 WORKLOAD = "causal_128k_balanced"
+L2_BYTES = 129 * 10**6  # GB300 L2 size
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
@@ -156,11 +157,12 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload or WORKLOAD]
     workload = WORKLOAD
-    if args.n or args.heads:
+    if args.workload or args.n or args.heads:
         w = w.with_(N=args.n or w.N, Hq=args.heads or w.Hq, Hkv=args.heads or w.Hkv)
-        workload = f"causal_{w.N}_h{w.Hq}_profiling"
+        workload = (f"{w.name}_n{w.N}_h{w.Hq}_profiling" if args.workload
+                    else f"causal_{w.N}_h{w.Hq}_profiling")
     x = make_inputs(w, device=dev, seed=w.seed + rank)
     q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
     o = torch.empty_like(q)
@@ -175,8 +177,8 @@ def run_ours(args, rank, world, local_rank):
         ctypes.byref(vq_), ctypes.byref(vk_), w.chunk, 1)), dtype=torch.uint8, device=dev)
 
     def step():
-        lsx.chunked_fwd(q, k, v, w.chunk, causal=True, out=o, lse=lse, workspace=ws_f)
-        lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=True, dq=dq, dk=dk, dv=dv,
+        lsx.chunked_fwd(q, k, v, w.chunk, causal=w.causal, out=o, lse=lse, workspace=ws_f)
+        lsx.chunked_bwd(q, k, v, o, lse, d_o, w.chunk, causal=w.causal, dq=dq, dk=dk, dv=dv,
                         workspace=ws)
 
     def barrier():
@@ -210,8 +212,9 @@ def run_ours(args, rank, world, local_rank):
     if lsx.sync_status() != 0:
         raise RuntimeError("device status after the timed steps")
 
-    f_fwd, f_bwd = flops(w.B, w.Hq, w.N, w.D)
+    f_fwd, f_bwd = flops(w.B, w.Hq, w.N, w.D, w.causal)
     step_flops = f_fwd + f_bwd
+    in_bytes = q.numel() * q.element_size()
     ms_max, value = job_throughput(ms, step_flops, args.steps, world, dev)
 
     # end to end through the same C ABI: every step copies its inputs in from
@@ -255,8 +258,9 @@ def run_ours(args, rank, world, local_rank):
                 stream.wait_event(ready[step_no % 2])
                 if step_no >= 2:  # step_no - 2's outputs (same buffers) are copied out
                     stream.wait_event(out_done[step_no % 2])
-                lsx.chunked_fwd(xq, xk, xv, w.chunk, causal=True, out=xo, lse=xl, workspace=ws_f)
-                lsx.chunked_bwd(xq, xk, xv, xo, xl, xdo, w.chunk, causal=True, dq=xdq, dk=xdk,
+                lsx.chunked_fwd(xq, xk, xv, w.chunk, causal=w.causal, out=xo, lse=xl,
+                                workspace=ws_f)
+                lsx.chunked_bwd(xq, xk, xv, xo, xl, xdo, w.chunk, causal=w.causal, dq=xdq, dk=xdk,
                                 dv=xdv, workspace=ws)
                 done[step_no % 2].record(stream)
                 s_out.wait_event(done[step_no % 2])
@@ -336,9 +340,11 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)*0.5 q/k/v, N(0,1) dO; one problem per rank)",
         "config": {"workload": workload, "B": w.B, "H": w.Hq, "N": w.N, "d": w.D,
-                   "chunk_len": w.chunk, "causal": True,
+                   "chunk_len": w.chunk, "causal": w.causal,
                    "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd,
-                   "l2": "inputs larger than L2 (q, k, v, dO 1 GiB each; no flush needed)",
+                   "l2": (f"inputs larger than L2 (q, k, v, dO {in_bytes / 2**30:.3g} GiB each; "
+                          "no flush needed)" if 4 * in_bytes > L2_BYTES else
+                          f"inputs of {4 * in_bytes / 2**20:.0f} MiB, within L2 (profiling case)"),
                    "pct_of_tensor_peak": round(100.0 * value / world / pk["bf16_sustained"], 2)},
         "roofline": roofline, "kernels": kernels, "secondary": sec, "cpu_baseline": cpu,
         "e2e": e2e,
@@ -614,6 +620,9 @@ def main():
     ap.add_argument("--n", type=int, default=None,
                     help="sequence length override (profiling captures on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="head count override (profiling)")
+    ap.add_argument("--workload", default=None,
+                    choices=("causal_32k_ring", "causal_128k_balanced", "noncausal_64k_heavytail"),
+                    help="another attention workload in place of the headline one (profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
