@@ -322,7 +322,8 @@ void lsx_set_wait_limit_ns(uint64_t ns);
 
 /* Backward reduction order.  on == 0 (the default): for bf16 inputs one kernel
  * computes dK, dV and dQ together and adds each key tile's contribution to
- * dQ into an fp32 accumulator with global atomic adds, so dQ's rounding
+ * dQ into an fp32 accumulator with reduce-adds (TMA bulk or vector atomic),
+ * performed at L2 in no fixed order, so dQ's rounding
  * depends on the order in which those adds land (results agree with the
  * deterministic mode within the documented tolerance, not bit for bit).
  * on != 0: dQ is computed by a second kernel in which every dQ row is owned

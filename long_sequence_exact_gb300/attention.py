@@ -264,7 +264,7 @@ def set_wait_limit_ns(ns: int) -> None:
 
 def set_deterministic(on: bool) -> None:
     """Select the backward's dQ reduction order (lsx_set_deterministic):
-    False (default) = fused dK/dV/dQ kernel adding dQ with fp32 atomics,
+    False (default) = fused dK/dV/dQ kernel adding dQ with fp32 reduce-adds,
     True = owner-computes dQ kernel, bitwise repeatable."""
     load().lsx_set_deterministic(1 if on else 0)
 

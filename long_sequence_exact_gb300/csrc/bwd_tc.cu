@@ -29,9 +29,15 @@
 //    With kDq and D = 64, TMEM has room to spare and shared memory too:
 //      dQ_i = dS K        (SS, both MN-major)     TMEM [320,384) / [448,512)
 //    alternating between the two free 64-column regions, with dS^T in its
-//    own double-buffered shared tile written before P^T is published; the
-//    grad warps read dQ_{i-1} back during step i and add it with 16-byte
-//    vector atomics (one query row per thread), so no product waits on it.
+//    own double-buffered shared tile written before P^T is published.  The
+//    MMA thread issues step i+1's S^T / dP^T ahead of dQ_i (dV and dK, the
+//    last readers of their columns, come first), so dQ_i runs under the
+//    grad warps' next step.  During step i+1 the grad warps read dQ_i back
+//    and stage it, scaled, in dS_i^T's spent tile as two swizzled [128
+//    queries][32 d] fp32 boxes; one thread of warp 2 adds them into the
+//    target with tensor-map reduce-adds and releases the tile for the dS^T
+//    of step i+2.  (Where the target takes no tensor map the grad warps add
+//    with 16-byte vector atomics instead.)
 //  * dq_kernel (the deterministic form of dQ), query-tile-major: a work item is one 128-row query tile; it
 //    walks every visible key tile:
 //      S  = Q K_j^T, dP = dO V_j^T (SS)                TMEM [0,128), [128,256)
