@@ -131,9 +131,11 @@ def test_fused_dq_agrees_with_owner_dq(grad_dtype):
             assert torch.equal(x, z) and torch.equal(x, y), name
 
 
-def test_fused_dq_adds_into_f32_dq():
-    # min workspace + f32 dq: the fused kernel adds straight into dq
-    q, k, v, d_o = make(1, 2, 2, 520, 640, 128, seed=33)
+@pytest.mark.parametrize("d", [128, 64])
+def test_fused_dq_adds_into_f32_dq(d):
+    # min workspace + f32 dq: the fused kernel adds straight into dq (at
+    # d = 64 through a tensor map over dq itself)
+    q, k, v, d_o = make(1, 2, 2, 520, 640, d, seed=33)
     o, lse = lsx.chunk_fwd(q, k, v, 120, 0, True)
     base = [torch.randn(t.shape, dtype=torch.float32, device=DEV) for t in (q, k, v)]
     outs = [t.clone() for t in base]
