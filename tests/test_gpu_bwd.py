@@ -41,6 +41,8 @@ CASES = [
     (1, 3, 1, 130, 700, 128, 1000, 600, True),
     (1, 2, 2, 128, 256, 128, 0, 64, True),   # rows and keys nobody pairs
     (1, 1, 1, 1000, 1000, 128, 0, 0, True),
+    (2, 4, 2, 200, 333, 64, 0, 0, False),    # d = 64: ragged tails, GQA
+    (1, 3, 1, 130, 700, 64, 1000, 600, True),
 ]
 
 
