@@ -39,13 +39,97 @@ WORKLOAD = "causal_128k_balanced"
 L2_BYTES = 129 * 10**6  # GB300 L2 size
 
 
-# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of each
-# tensor-core kernel on the 128K workload, from single-pass ncu captures of
-# this bench (--steps 1 --warmup 1).  They describe the kernels as they were
-# captured and are re-taken whenever a kernel changes (bwd_dkdv_tc and
-# bwd_dq_tc: the deterministic-mode kernels, from an earlier capture).
-DRAM_BYTES_128K = {"fwd_tc": 38.73e9 + 1.41e9, "bwd_fused_tc": 52.09e9 + 27.06e9,
-                   "bwd_dkdv_tc": 42.16e9 + 2.15e9, "bwd_dq_tc": 39.92e9 + 1.07e9}
+PKG = os.path.join(ROOT, "long_sequence_exact_gb300")
+# Source files whose text fixes each tensor-core kernel's code: a DRAM figure
+# taken by ncu is used only while the hash of these files is the one recorded
+# beside it (profiles/*.md, "traffic:" lines), so a changed kernel reports no
+# stale traffic.
+KERNEL_SOURCES = {
+    "fwd_tc": ("csrc/fwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+    "bwd_fused_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+    "bwd_dkdv_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+    "bwd_dq_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+}
+TRACE_KERNELS = {0: "fwd_tc", 1: "bwd_dkdv_tc", 2: "bwd_dq_tc", 12: "bwd_fused_tc"}
+
+
+def kernel_source_hash(name):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[name]:
+        with open(os.path.join(PKG, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def tile_pairs(b, h, n, causal=True):
+    """(query tile, key tile) pairs of 128 x 128 that the kernels visit."""
+    t = (n + 127) // 128
+    return b * h * (t * (t + 1) // 2 if causal else t * t)
+
+
+def recorded_traffic(name, units):
+    """DRAM bytes per launch of kernel `name` scaled to `units` tile pairs,
+    from a committed ncu summary whose source hash matches the current
+    kernel source; None when there is none (never taken, or the kernel has
+    changed since).  A profiles/*.md line reads
+      traffic: kernel=<name> source=<hash16> bytes=<dram read+write> units=<tile pairs>"""
+    import glob
+    import re
+    want = kernel_source_hash(name)
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as f:
+            for line in f:
+                m = re.match(r"\s*traffic:\s*kernel=(\S+)\s+source=(\S+)\s+bytes=(\S+)\s+units=(\S+)",
+                             line)
+                if m and m.group(1) == name and m.group(2) == want:
+                    return {"bytes": float(m.group(3)) / float(m.group(4)) * units,
+                            "source": os.path.relpath(path, ROOT), "captured_units": float(m.group(4))}
+    return None
+
+
+def parse_trace(words):
+    """Per-launch records written by the persistent kernels (lsx_trace_enable):
+    [kid, G, items] then (start_ns, end_ns, items) per CTA.  Returns a list of
+    dicts with the SM idle fraction 1 - sum(busy) / (G * makespan)."""
+    out, i = [], 0
+    while i + 3 <= len(words):
+        kid, g, items = int(words[i]), int(words[i + 1]), int(words[i + 2])
+        if g <= 0 or i + 3 + 3 * g > len(words):
+            break
+        cta = [(int(words[i + 3 + 3 * c]), int(words[i + 4 + 3 * c]), int(words[i + 5 + 3 * c]))
+               for c in range(g)]
+        t0 = min(c[0] for c in cta)
+        t1 = max(c[1] for c in cta)
+        span = max(t1 - t0, 1)
+        busy = sum(c[1] - c[0] for c in cta)
+        ends = sorted(c[1] - t0 for c in cta)
+        out.append({"kernel": TRACE_KERNELS.get(kid, str(kid)), "ctas": g, "items": items,
+                    "items_run": sum(c[2] for c in cta),
+                    "makespan_ms": round(span / 1e6, 3),
+                    "idle_fraction": round(1.0 - busy / (g * span), 4),
+                    "first_cta_done_ms": round(ends[0] / 1e6, 3),
+                    "median_cta_done_ms": round(ends[g // 2] / 1e6, 3)})
+        i += 3 + 3 * g
+    return out
+
+
+def traced(step, dev):
+    """Runs `step` once with the schedule trace on; returns parse_trace's list."""
+    import torch
+    from long_sequence_exact_gb300 import _lib
+    lib = _lib.load()
+    buf = torch.zeros(1 << 17, dtype=torch.int64, device=dev)
+    torch.cuda.synchronize()
+    _lib.check(lib.lsx_trace_enable(buf.data_ptr(), buf.numel() * 8), "lsx_trace_enable")
+    try:
+        step()
+        torch.cuda.synchronize()
+        used = lib.lsx_trace_used() // 8
+    finally:
+        lib.lsx_trace_enable(None, 0)
+    words = buf[:used].cpu().tolist()
+    return parse_trace(words)
 
 
 def job_throughput(ms_local, work_per_step, steps, world, device="cpu"):
@@ -72,9 +156,12 @@ def peaks():
     if os.path.exists(path):
         with open(path) as f:
             m = json.load(f)
+        clk = (m.get("clocks_under_load") or {}).get("sm_mhz_median")
         return {"hbm_gbs": m["hbm_gbs"], "bf16": m["bf16_tflops"],
-                "bf16_sustained": m["bf16_tflops_sustained"], "source": "measured"}
-    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+                "bf16_sustained": m["bf16_tflops_sustained"], "source": "measured",
+                "sustained_sm_mhz": clk}
+    return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback",
+            "sustained_sm_mhz": None}
 
 
 class ClockSampler:
@@ -296,10 +383,13 @@ def run_ours(args, rank, world, local_rank):
     # fwd_tc = the two forward GEMMs; bwd_fused_tc = all 5 backward GEMMs
     # (S^T, dP^T, dV, dK, dQ); in the deterministic mode bwd_dkdv_tc = S^T,
     # dP^T, dV, dK (4 of 5) and bwd_dq_tc = dQ (1 of 5; its S and dP are
-    # recomputed)
+    # recomputed).  Fractions are given against both measured peaks: the
+    # sustained one (a long cuBLAS loop under the power cap, the reference for
+    # kernels timed inside a long step) and the burst one.
     unit_gemm = f_fwd / 2.0
     algo = {"fwd_tc": 2 * unit_gemm, "bwd_fused_tc": 5 * unit_gemm,
             "bwd_dkdv_tc": 4 * unit_gemm, "bwd_dq_tc": 1 * unit_gemm}
+    units = tile_pairs(w.B, w.Hq, w.N, w.causal)
     dom = max(ktimes.items(), key=lambda kv: kv[1][1]) if ktimes else None
     roofline = None
     kernels = {}
@@ -310,24 +400,35 @@ def run_ours(args, rank, world, local_rank):
             ach = algo[name] / (avg / 1e3) / 1e12
             ent["achieved_tflops"] = round(ach, 1)
             ent["frac_of_peak"] = round(ach / pk["bf16_sustained"], 4)
+            ent["frac_of_burst_peak"] = round(ach / pk["bf16"], 4)
+            rec = recorded_traffic(name, units) if name in KERNEL_SOURCES else None
+            ent["dram_bytes_per_launch"] = round(rec["bytes"]) if rec else None
         kernels[name] = ent
-    for name in kernels:
-        if workload == WORKLOAD and name in DRAM_BYTES_128K:
-            kernels[name]["dram_bytes_per_launch"] = DRAM_BYTES_128K[name]
     if dom is not None and dom[0] in algo:
-        traffic = args.traffic
-        if traffic is None and workload == WORKLOAD:
-            traffic = DRAM_BYTES_128K.get(dom[0])
         name, (cnt, tot) = dom
+        rec = recorded_traffic(name, units)
+        traffic = args.traffic if args.traffic is not None else (round(rec["bytes"]) if rec else None)
         ach = algo[name] / (tot / cnt / 1e3) / 1e12
         roofline = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),
                     "peak": pk["bf16_sustained"], "unit": "TFLOP/s",
                     "frac": round(ach / pk["bf16_sustained"], 4), "traffic": traffic,
-                    "peak_kind": f"{pk['source']} bf16 sustained (kernel timed inside a long step)"}
+                    "peak_kind": f"{pk['source']} bf16 sustained (kernel timed inside a long step)",
+                    "peak_burst": pk["bf16"], "frac_of_burst": round(ach / pk["bf16"], 4),
+                    "peak_sustained_sm_mhz": pk.get("sustained_sm_mhz"),
+                    "traffic_source": (rec["source"] + f" (ncu capture of {rec['captured_units']:.0f} "
+                                       f"tile pairs, scaled to {units} by tile pairs)")
+                    if rec and args.traffic is None else
+                    ("--traffic" if args.traffic is not None else
+                     "none for the current kernel source")}
+
+    # SM idle fraction of the persistent kernels: one more (untimed) step
+    # with the device-side schedule trace on
+    schedule = traced(step, dev) if not args.no_trace else None
 
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        cpu = cpu_baseline(args.cpu_rows)
+        cpu = cpu_baseline(repeats=args.cpu_repeats)
+        cpu["gpu_step_s"] = round(ms_max / args.steps / 1e3, 4)
     sec = None
     if not args.no_secondary:
         del q, k, v, d_o, o, lse, dq, dk, dv, ws, ws_f, x
@@ -345,8 +446,10 @@ def run_ours(args, rank, world, local_rank):
                    "l2": (f"inputs larger than L2 (q, k, v, dO {in_bytes / 2**30:.3g} GiB each; "
                           "no flush needed)" if 4 * in_bytes > L2_BYTES else
                           f"inputs of {4 * in_bytes / 2**20:.0f} MiB, within L2 (profiling case)"),
-                   "pct_of_tensor_peak": round(100.0 * value / world / pk["bf16_sustained"], 2)},
-        "roofline": roofline, "kernels": kernels, "secondary": sec, "cpu_baseline": cpu,
+                   "pct_of_tensor_peak": round(100.0 * value / world / pk["bf16_sustained"], 2),
+                   "pct_of_burst_tensor_peak": round(100.0 * value / world / pk["bf16"], 2)},
+        "roofline": roofline, "kernels": kernels, "schedule": schedule, "secondary": sec,
+        "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": sum(c for c, _ in ktimes.values()),
         "clocks": clk.summary(),
@@ -356,7 +459,9 @@ def run_ours(args, rank, world, local_rank):
 # ----------------------------------------------- bandwidth-bound rows
 def secondary(dev, pk):
     """Rows of the path other than the headline, timed alone with CUDA events
-    (median of 5 after 3 warm-ups; every input is larger than L2):
+    (median of 5 after 3 warm-ups; every input is larger than L2; the
+    attention workloads also report their SM idle fractions from one more
+    traced, untimed step):
       merge       attn_merge of two fp32 partials at the 128K row count
                   (B=1, H=32, N=131072, d=128): reads 2 x (O + LSE), writes 1
       tree_merge  attn_tree_merge of 8 fp32 partials at the 32K row count
@@ -451,7 +556,9 @@ def secondary(dev, pk):
         ff, fb = flops(w.B, w.Hq, w.N, w.D, causal)
         tf = (ff + fb) / (ms / 1e3) / 1e12
         out[name] = {"tflops": round(tf, 1), "frac": round(tf / pk["bf16_sustained"], 4),
+                     "frac_of_burst": round(tf / pk["bf16"], 4),
                      "ms": round(ms, 3), "flops": ff + fb,
+                     "schedule": traced(fwd_bwd, dev),
                      "workload": f"B={w.B} H={w.Hq} N={w.N} d={w.D} chunk={w.chunk} "
                                  f"{'causal' if causal else 'non-causal'}"}
         del x, q, k, v, d_o, o, lse, grads
@@ -546,60 +653,104 @@ def secondary(dev, pk):
 
 
 # ------------------------------------------------------------ CPU oracle
-def cpu_baseline(rows_per_sample=512, repeats=1):
-    """The fp64 oracle as it stands, on the host cores, on a bounded sample:
-    the last `rows_per_sample` query rows of head 0 of the 128K workload
-    (each sees ~131K keys), forward + backward.  Value in the metric's unit
-    (TFLOP/s by the same visible-pair convention)."""
+CPU_ROWS_PER_HEAD = 16   # seeded random query rows in every head ...
+CPU_TAIL_ROWS = 256      # ... plus the last rows of head 0
+
+
+def cpu_sample():
+    """The bounded sample of the 128K workload that both CPU legs time: for
+    each of the 32 heads, 16 seeded random query rows, plus the last 256 query
+    rows of head 0 (the rows that see the most keys).  Each head's q, k, v, dO
+    are drawn with their own seed at the workload's scale (N(0,1)*0.5 for q,
+    k, v; N(0,1) for dO).  Returns [(rows, q, k, v, d_o) per head] as fp64
+    arrays of the bf16 values and the FLOPs the sample stands for (visible
+    pairs only, forward + 2.5x backward)."""
     import numpy as np
     import torch
 
-    from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs
-    from oracle import attention as A
+    from long_sequence_exact_gb300.inputs import WORKLOADS, random_tensor
 
-    cores = len(os.sched_getaffinity(0))
-    torch.set_num_threads(cores)
-    w = WORKLOADS[WORKLOAD].with_(Hq=1, Hkv=1)
-    x = make_inputs(w, device="cpu")
+    w = WORKLOADS[WORKLOAD]
+    rng = np.random.default_rng(w.seed)
     f = lambda t: t.double().numpy()  # noqa: E731
-    q, k, v, d_o = f(x["q"]), f(x["k"]), f(x["v"]), f(x["d_o"])
-    rows = np.arange(w.N - rows_per_sample, w.N)
+    heads, flops_ = [], 0.0
+    for h in range(w.Hq):
+        rows = np.sort(rng.choice(w.N, size=CPU_ROWS_PER_HEAD, replace=False))
+        if h == 0:
+            rows = np.union1d(rows, np.arange(w.N - CPU_TAIL_ROWS, w.N))
+        base = w.seed * 1000 + 4 * h
+        q, k, v = (f(random_tensor((1, 1, w.N, w.D), base + i, w.qk_amp, torch.bfloat16))
+                   for i in range(3))
+        d_o = f(random_tensor((1, 1, w.N, w.D), base + 3, 1.0, torch.bfloat16))
+        heads.append((rows, q, k, v, d_o))
+        flops_ += 4.0 * float(np.sum(rows + 1)) * w.D * 3.5
+    return heads, flops_
+
+
+def time_cpu_sample(sample):
+    """Wall seconds of the fp64 oracle's forward + backward over the sample."""
+    from oracle import attention as A
+    heads, _ = sample
     t0 = time.perf_counter()
-    for _ in range(repeats):
+    for rows, q, k, v, d_o in heads:
         A.attn_fwd(q, k, v, 0, 0, True, rows=rows)
         A.attn_bwd(q, k, v, d_o, 0, 0, True, rows=rows)
-    dt = (time.perf_counter() - t0) / repeats
-    pairs = float(sum(r + 1 for r in rows))
-    fl = 4.0 * pairs * w.D * 3.5  # fwd + 2.5x fwd
-    return {"value": round(fl / dt / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"fp64 numpy oracle, fwd+bwd of the last {rows_per_sample} query rows of "
-                      f"head 0 (N={w.N}, d={w.D}, causal), {dt:.2f} s",
-            "seconds": round(dt, 3)}
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(repeats=4, sample=None):
+    """The fp64 oracle as it stands, on the host cores, timed on cpu_sample()
+    `repeats` times.  Value in the metric's unit (TFLOP/s by the same visible-
+    pair convention), with the labelled extrapolation of that rate to one full
+    step of the 128K workload."""
+    import torch
+    cores = len(os.sched_getaffinity(0))
+    torch.set_num_threads(cores)
+    sample = sample or cpu_sample()
+    dt = sum(time_cpu_sample(sample) for _ in range(repeats)) / repeats
+    rate = sample[1] / dt
+    f_fwd, f_bwd = flops(1, 32, 131072, 128, True)
+    n_rows = sum(len(h[0]) for h in sample[0])
+    return {"value": round(rate / 1e12, 6), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"fp64 numpy oracle, fwd+bwd of {n_rows} query rows of the causal 128K "
+                       f"workload ({CPU_ROWS_PER_HEAD} seeded random rows in each of the 32 heads "
+                       f"+ the last {CPU_TAIL_ROWS} rows of head 0), {dt:.2f} s per pass, "
+                       f"{repeats} passes"),
+            "seconds": round(dt, 3),
+            "extrapolated_full_step_s": round((f_fwd + f_bwd) / rate, 1),
+            "extrapolation": "full 128K fwd+bwd FLOPs / the sample's rate (not run)"}
 
 
 def run_reference(args, rank):
     if rank != 0:
         return None
+    import torch
     cores = len(os.sched_getaffinity(0))
-    # each reference step is a quarter of the main arm's sample (a few
-    # seconds), so that --steps K --warmup W ends within minutes
+    torch.set_num_threads(cores)
+    sample = cpu_sample()  # the same sample as the main arm's cpu_baseline leg
     for _ in range(args.warmup):
-        cpu_baseline(max(1, args.cpu_rows // 16))
-    vals = []
-    t0 = time.perf_counter()
+        time_cpu_sample(sample)
+    ts = []
     for _ in range(args.steps):
-        vals.append(cpu_baseline(max(1, args.cpu_rows // 4)))
-    total = time.perf_counter() - t0
-    value = statistics.mean(v["value"] for v in vals)
+        ts.append(time_cpu_sample(sample))
+    total = sum(ts)
+    value = sample[1] * len(ts) / total / 1e12
+    f_fwd, f_bwd = flops(1, 32, 131072, 128, True)
+    n_rows = sum(len(h[0]) for h in sample[0])
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": WORKLOAD, "B": 1, "H": 32, "N": 131072,
                                         "d": 128, "chunk_len": 4096, "causal": True},
-        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": cores,
-                         "sample": vals[0]["sample"]},
-        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "kind": "oracle", "cores": cores,
+                         "sample": (f"fp64 numpy oracle, fwd+bwd of {n_rows} query rows of the "
+                                    f"causal 128K workload ({CPU_ROWS_PER_HEAD} seeded random rows "
+                                    f"in each of the 32 heads + the last {CPU_TAIL_ROWS} rows of "
+                                    "head 0) per step"),
+                         "extrapolated_full_step_s": round((f_fwd + f_bwd) / (value * 1e12), 1)},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
     }
 
 
@@ -609,9 +760,11 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=3072,
-                    help="query rows in the oracle's CPU sample (about 10 s on 16 cores)")
+    ap.add_argument("--cpu-repeats", type=int, default=4,
+                    help="passes over the oracle's CPU sample (about 2.5 s each on 16 cores)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-trace", action="store_true",
+                    help="skip the untimed step that records the SM idle fraction")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the merge / tree-merge / decode bandwidth rows")

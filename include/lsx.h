@@ -222,11 +222,18 @@ int attn_block_sparse_bwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_te
  *    size (B * Hq * Lq <= 4,194,304 query rows); larger problems return
  *    LSX_ERR_WORKSPACE and launch nothing.
  *  - The array is shared by every call on a device and keeps the last
- *    call's contents (nothing in it needs to start at zero).  Calls whose
- *    work overlaps on the GPU race on it: order them on one stream.
+ *    call's contents.  Each call rewrites what it reads (the row sums and
+ *    statistics by its row-dot kernel; the fp32 dQ accumulator, when it fits,
+ *    is cleared on the call's stream by cudaMemsetAsync, which allocates
+ *    nothing).  Calls whose work overlaps on the GPU race on it: order them
+ *    on one stream.
  *  - The first call on a device, with that device current, looks up the
  *    array's device address (cudaGetSymbolAddress) and caches it; make that
- *    first call before any stream capture.
+ *    first call before any stream capture.  With CUDA's default lazy module
+ *    loading, that first call (or the first kernel of this library on the
+ *    device) is also when the driver loads the library onto the device and
+ *    reserves the 16 MiB: callers that may not take device memory after
+ *    their start-up should make one call during start-up.
  *  - Allocates nothing (no cudaMalloc / cudaFree / allocating library call).
  * ---------------------------------------------------------------------- */
 size_t attn_chunk_bwd_noalloc_max_bytes(void);
@@ -243,11 +250,16 @@ int attn_chunk_bwd_noalloc(const lsx_tensor* q, const lsx_tensor* k,
  * into chunks of chunk_len rows, every (query chunk, key chunk) pair that the
  * mask leaves visible computed in ONE persistent launch whose CTAs take
  * work items from a longest-first causal schedule (DistFlashAttn, core
- * concepts: load-balanced scheduling; here the workers are the SMs).  Query
- * rows whose key range is long may be split into pieces whose partials are
- * combined by the tree merge (Lean Attention abstract: stream-K style
- * reduction); workspace then holds those partials.
- * chunk_len must be a multiple of 128.  Same dtypes as the chunk calls.
+ * concepts: load-balanced scheduling; here the workers are the SMs).
+ * chunk_len is validated (a positive multiple of 128) but is not a kernel
+ * boundary: a work item walks the key tiles of consecutive chunks without
+ * stopping, carrying one online softmax across the chunk edges, which equals
+ * computing each chunk pair's partial and combining the partials with
+ * attn_merge in that order (the merge is associative: Lean Attention
+ * abstract).  No partials are written and no row is split; the forward
+ * workspace holds only the key-contiguous copy of V (as attn_chunk_fwd), the
+ * backward workspace what attn_chunk_bwd uses.  Same dtypes as the chunk
+ * calls.
  * ---------------------------------------------------------------------- */
 size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal);
@@ -346,6 +358,28 @@ int lsx_selftest_bounded_wait(lsx_stream_t stream);
  * up) and the total into out[0..2].  host pointers. */
 int lsx_schedule_stats(int64_t B, int64_t H, int64_t N, int64_t chunk_len,
                        int causal, int n_workers, int64_t* out);
+
+/* Device-side record of the balanced causal schedule (DistFlashAttn, core
+ * concepts: load-balanced scheduling removes the idle time of the workers
+ * that finish early; here the workers are the SMs of one GPU).  While a trace
+ * buffer is set, every launch of a persistent tensor-core kernel (the
+ * forward, the fused or the dK/dV backward, the deterministic dQ kernel)
+ * appends one record to it, written by the kernel itself:
+ *   uint64 words [0] kernel id (0 forward, 1 dK/dV, 2 dQ, 12 fused dK/dV/dQ),
+ *   [1] G = CTAs in the launch, [2] work items in the launch, then for each
+ *   CTA c: [3 + 3c] its %globaltimer (ns) before its first item, [4 + 3c]
+ *   after its last item (every role done), [5 + 3c] the items it ran.
+ * The SM idle fraction of a launch is 1 - sum_c (end_c - start_c) /
+ * (G * (max end - min start)).
+ *   buf: DEVICE memory owned by the caller, 8-byte aligned, or NULL to stop
+ *   tracing; bytes: its size.  A launch whose record would not fit is not
+ *   traced (not an error).  Enabling resets the fill level to 0.
+ * lsx_trace_used returns the bytes handed out to records since the last
+ * lsx_trace_enable (read the buffer after the launches have completed).
+ * Process-wide and for diagnosis only: costs one predicated branch per CTA
+ * when off, two %globaltimer reads and 24 bytes per CTA when on. */
+int lsx_trace_enable(void* buf, size_t bytes);
+size_t lsx_trace_used(void);
 
 /* Library version string, e.g. "lsx 0.1 sm_103a". */
 const char* lsx_version(void);

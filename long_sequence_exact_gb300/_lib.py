@@ -83,6 +83,8 @@ SIGNATURES = {
     "lsx_set_deterministic": (None, [_INT]),
     "lsx_selftest_bounded_wait": (_INT, [_VP]),
     "lsx_schedule_stats": (_INT, [_I64, _I64, _I64, _I64, _INT, _INT, ctypes.POINTER(_I64)]),
+    "lsx_trace_enable": (_INT, [_VP, _SZ]),
+    "lsx_trace_used": (_SZ, []),
     "lsx_version": (ctypes.c_char_p, []),
     "lsx_timing_enable": (_INT, [_INT]),
     "lsx_timing_report": (_INT, [ctypes.c_char_p, _SZ]),

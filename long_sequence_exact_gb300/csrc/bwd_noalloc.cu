@@ -13,18 +13,26 @@
 // The array is a file-scope __device__ variable of kNoAllocScratchBytes
 // (16 MiB: delta for up to 4,194,304 query rows, e.g. 32 heads x 131,072
 // tokens).  Every GPU that loads the library keeps it until the process
-// exits.  When the sequence-contiguous operand copies that attn_chunk_bwd
-// makes for its faster path also fit, they go into the same array.  It is
-// shared by all calls on a device and keeps the last call's contents;
-// nothing in it has to start at zero, because the row-dot and copy kernels
-// write every entry a call uses before the backward kernels read it.
-// Two calls whose work overlaps on the GPU (e.g. on two streams without an
-// ordering between them) race on the array and produce wrong gradients.
+// exits.  When the row statistics and the fp32 dQ accumulator (or the
+// sequence-contiguous copy of K) that attn_chunk_bwd uses for its faster
+// path also fit, they go into the same array.  It is shared by all calls on
+// a device and keeps the last call's contents.  What a call reads is
+// written by that call first: the row-dot kernel rewrites the delta rows,
+// the row statistics and the selector tiles; the K copy is rewritten by the
+// transpose kernel; the dQ accumulator is cleared on the call's stream by
+// the backward itself (cudaMemsetAsync, which allocates nothing) before the
+// fused kernel adds into it.  Two calls whose work overlaps on the GPU (e.g.
+// on two streams without an ordering between them) race on the array and
+// produce wrong gradients.
 //
 // Set-up: the first call made on a device (with that device current) looks
 // up the device address of the array with cudaGetSymbolAddress and caches
-// it; that first call should come before any stream capture.  No call
-// allocates: no cudaMalloc, cudaFree or allocating library routine.
+// it; that first call should come before any stream capture.  Under CUDA's
+// default lazy module loading, that look-up (or the first kernel of this
+// library run on the device) is also when the driver loads the library's
+// module on that device and reserves the 16 MiB; a caller that must not
+// take device memory after its start-up makes one small call during start-up.
+// No call allocates: no cudaMalloc, cudaFree or allocating library routine.
 #include <mutex>
 
 #include "internal.h"

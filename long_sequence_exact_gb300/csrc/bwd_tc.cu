@@ -103,6 +103,8 @@ struct BwdParams {
   float* dq_acc;
   int64_t acc_sb, acc_sh, acc_sn;
   int acc_tma;
+  uint64_t* trace;  // per-CTA schedule record (NULL: not traced)
+  int trace_kid;
 };
 
 // Row pitch (elements) of the transposed fp32 dQ accumulator [.][128][Np]:
@@ -396,6 +398,8 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
+  if (p.trace != nullptr && threadIdx.x == 0)
+    trace_begin(p.trace, p.trace_kid, p.n_items, global_timer_ns());
 
   // 640 threads launched at <= 96 registers (61,440): the load/MMA
   // warpgroup keeps 64, the four grad warpgroups take 104:
@@ -410,7 +414,8 @@ __global__ void __launch_bounds__(640, 1)
         tma_load_4d(sm.ones[0], &tm_ones, &sm.ones_full, 0, 0, 0, 0);
         tma_load_4d(sm.ones[1], &tm_ones, &sm.ones_full, 0, 128, 0, 0);
       }
-      for (int64_t r = 0;; ++r) {
+      int64_t r = 0;
+      for (;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
         const DkdvItem x = dkdv_item(p, it);
@@ -461,6 +466,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         if (!ok) break;
       }
+      if (p.trace != nullptr && lane == 0) trace_items(p.trace, r);
     } else if (warp == 1 && lane == 0) {
       // ----------------------------------------------------------- MMA issue
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
@@ -936,6 +942,7 @@ __global__ void __launch_bounds__(640, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.trace != nullptr && threadIdx.x == 0) trace_end(p.trace, global_timer_ns());
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -1028,6 +1035,8 @@ __global__ void __launch_bounds__(640, 1)
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x, c = blockIdx.x;
+  if (p.trace != nullptr && threadIdx.x == 0)
+    trace_begin(p.trace, p.trace_kid, p.n_items, global_timer_ns());
 
   // 640 threads launched at <= 96 registers (61,440): the load/MMA
   // warpgroup keeps 64, the four grad warpgroups take 104:
@@ -1037,7 +1046,8 @@ __global__ void __launch_bounds__(640, 1)
     if (warp == 0 && lane == 0) {
       // ------------------------------------------- loads: Q, dO and K/V ring
       uint32_t stage = 0, phase = 0, qo_phase = 0;
-      for (int64_t r = 0;; ++r) {
+      int64_t r = 0;
+      for (;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
         const DqItem x = dq_item(p, it);
@@ -1058,6 +1068,7 @@ __global__ void __launch_bounds__(640, 1)
         }
         if (!ok) break;
       }
+      if (p.trace != nullptr) trace_items(p.trace, r);
     } else if (kT && warp == 0 && lane == 1) {
       // ------------------------- loads: K^T ring (its own thread, so that a
       // K^T slot still in use never holds back the K/V prefetch)
@@ -1233,6 +1244,7 @@ __global__ void __launch_bounds__(640, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.trace != nullptr && threadIdx.x == 0) trace_end(p.trace, global_timer_ns());
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -1389,6 +1401,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.col_list = bl ? bl->col_list : nullptr;
   p.dq_acc = nullptr;
   p.acc_sb = p.acc_sh = p.acc_sn = 0;
+  p.trace = nullptr;
+  p.trace_kid = 0;
 
   // dK, dV (and dQ): items (key tile, b, kv head)
   p.n_items = p.n_ktiles * q.B * k.H;
@@ -1431,6 +1445,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    p.trace_kid = kKidBwdFused;
+    p.trace = trace_record(kKidBwdFused, grid);
     timing_begin(kKidBwdFused, s);
     kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, tacc, p);
     timing_end(kKidBwdFused, s);
@@ -1462,6 +1478,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    p.trace_kid = kKidDkdv;
+    p.trace = trace_record(kKidDkdv, grid);
     timing_begin(kKidDkdv, s);
     kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, tk, p);
     timing_end(kKidDkdv, s);
@@ -1476,6 +1494,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
     const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+    p.trace_kid = kKidDq;
+    p.trace = trace_record(kKidDq, grid);
     timing_begin(kKidDq, s);
     kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, tkt, p);
     timing_end(kKidDq, s);

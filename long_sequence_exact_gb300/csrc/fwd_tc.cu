@@ -94,6 +94,7 @@ struct FwdParams {
   const int32_t* pair_list;
   const uint8_t* bmask;  // [n_qtiles][n_kb]
   int64_t n_qtiles, n_kb;
+  uint64_t* trace;  // per-CTA schedule record (NULL: not traced)
 };
 
 struct Item {
@@ -177,6 +178,8 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = sm.tmem_base;
   const int64_t G = gridDim.x;
   const int64_t c = blockIdx.x;
+  if (p.trace != nullptr && threadIdx.x == 0)
+    trace_begin(p.trace, kKidFwdTc, p.n_items, global_timer_ns());
   // 384 threads launched at <= 168 registers (64,512).  Producer/MMA
   // warpgroup keeps 104 (the issuing thread spills with less, and it is on
   // the critical path), the two softmax warpgroups take 200:
@@ -186,7 +189,8 @@ __global__ void __launch_bounds__(384, 1)
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     uint32_t stage = 0, phase = 0, qe_phase = 0;
-    for (int64_t r = 0;; ++r) {
+    int64_t r = 0;
+    for (;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
       const Item x = decode_item(p, it);
@@ -226,6 +230,7 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
     }
+    if (p.trace != nullptr) trace_items(p.trace, r);
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------- MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
@@ -525,6 +530,7 @@ __global__ void __launch_bounds__(384, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (p.trace != nullptr && threadIdx.x == 0) trace_end(p.trace, global_timer_ns());
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
@@ -578,6 +584,7 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
                            static_cast<int>(smem)) != cudaSuccess)
     return LSX_ERR_LAUNCH;
   const int64_t grid = p.n_items < ctx.sm_count ? p.n_items : ctx.sm_count;
+  p.trace = trace_record(kKidFwdTc, grid);
   timing_begin(kKidFwdTc, s);
   kern<<<static_cast<unsigned>(grid), 384, smem, s>>>(tq, tk, tv, p);
   timing_end(kKidFwdTc, s);

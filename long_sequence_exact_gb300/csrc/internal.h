@@ -36,6 +36,37 @@ int launch_transpose(const lsx_tensor& in, void* out, cudaStream_t s);
 void timing_begin(int kid, cudaStream_t s);
 void timing_end(int kid, cudaStream_t s);
 
+// Optional per-CTA trace of the persistent kernels (lsx_trace_enable).  A
+// launch of kernel `kid` on `grid` CTAs asks for a record; NULL means no
+// tracing (disabled, or the caller's buffer is full).  The kernel writes the
+// record itself: words [0..2] = kid, grid, work items; then for CTA c the
+// words [3 + 3c .. 5 + 3c] = %globaltimer when it starts its first item,
+// %globaltimer when it has finished its last, and the items it ran.
+uint64_t* trace_record(int kid, int64_t grid);
+constexpr int64_t trace_words(int64_t grid) { return 3 + 3 * grid; }
+
+// Record writes, by thread 0 of each CTA: trace_begin after the set-up,
+// trace_items when its loader has gone through its items, trace_end once
+// every role has left its loop.
+__device__ __forceinline__ uint64_t* trace_cta(uint64_t* rec) {
+  return rec + 3 + 3 * static_cast<int64_t>(blockIdx.x);
+}
+__device__ __forceinline__ void trace_begin(uint64_t* rec, int kid, int64_t n_items,
+                                            uint64_t now) {
+  if (blockIdx.x == 0) {
+    rec[0] = static_cast<uint64_t>(kid);
+    rec[1] = gridDim.x;
+    rec[2] = static_cast<uint64_t>(n_items);
+  }
+  trace_cta(rec)[0] = now;
+}
+__device__ __forceinline__ void trace_items(uint64_t* rec, int64_t done) {
+  trace_cta(rec)[2] = static_cast<uint64_t>(done);
+}
+__device__ __forceinline__ void trace_end(uint64_t* rec, uint64_t now) {
+  trace_cta(rec)[1] = now;
+}
+
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // Element offset of (b, h, n, 0) in a view.

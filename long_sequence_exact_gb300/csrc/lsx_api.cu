@@ -81,6 +81,25 @@ void timing_end(int kid, cudaStream_t s) {
   g_open_ev = nullptr;
 }
 
+namespace {
+// ------------------------------------------------------- schedule trace
+std::mutex g_trmu;
+uint64_t* g_trace_buf = nullptr;  // caller's device buffer (words)
+size_t g_trace_cap = 0;           // words
+size_t g_trace_used = 0;          // words handed out since lsx_trace_enable
+}  // namespace
+
+uint64_t* trace_record(int kid, int64_t grid) {
+  (void)kid;
+  std::lock_guard<std::mutex> lk(g_trmu);
+  if (g_trace_buf == nullptr) return nullptr;
+  const size_t need = static_cast<size_t>(trace_words(grid));
+  if (g_trace_used + need > g_trace_cap) return nullptr;
+  uint64_t* rec = g_trace_buf + g_trace_used;
+  g_trace_used += need;
+  return rec;
+}
+
 int device_ctx(DeviceCtx* ctx) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return LSX_ERR_DEVICE;
@@ -674,6 +693,21 @@ int lsx_timing_report(char* buf, size_t n) {
     ++reported;
   }
   return reported;
+}
+
+// --------------------------------------------------------- schedule trace
+int lsx_trace_enable(void* buf, size_t bytes) {
+  std::lock_guard<std::mutex> lk(g_trmu);
+  if (buf != nullptr && reinterpret_cast<uintptr_t>(buf) % 8 != 0) return LSX_ERR_ALIGN;
+  g_trace_buf = static_cast<uint64_t*>(buf);
+  g_trace_cap = buf == nullptr ? 0 : bytes / sizeof(uint64_t);
+  g_trace_used = 0;
+  return LSX_OK;
+}
+
+size_t lsx_trace_used(void) {
+  std::lock_guard<std::mutex> lk(g_trmu);
+  return g_trace_used * sizeof(uint64_t);
 }
 
 // ------------------------------------------------------------ diagnostics

@@ -117,3 +117,10 @@ def test_decode_validation(lib):
                            R(_lse(b=2, h=16, n=1)), None, 0, None) == -5   # group of 16
     assert lib.attn_decode(R(q), R(kc), R(kc), 100, -1.0, R(o), R(l), None, 0, None) == -5
     assert lib.attn_decode(R(q), R(kc), R(kc), 4096, -1.0, R(o), R(l), None, 0, None) == -6
+
+
+def test_trace_buffer_validation(lib):
+    # host-side bookkeeping only: nothing is launched
+    assert lib.lsx_trace_enable(ctypes.c_void_p(0x10004), 4096) == -4  # not 8-byte aligned
+    assert lib.lsx_trace_enable(None, 0) == 0
+    assert lib.lsx_trace_used() == 0

@@ -18,7 +18,8 @@ import torch
 from oracle import attention as A
 import long_sequence_exact_gb300 as lsx
 from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs
-from helpers import TOL_GRAD_REL, TOL_LSE_BF16, TOL_O_BF16, check_close, check_lse, f64, rel_fro
+from helpers import (TOL_GRAD_REL, TOL_LSE_BF16, TOL_O_BF16, check_close, check_lse, check_tiles, f64,
+                     oracle_bwd_rows, rel_fro)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -56,13 +57,18 @@ def test_causal_128k_balanced_full_size():
         o_ref, lse_ref = A.attn_fwd(qh, kh, vh, 0, 0, True, rows=rows)
         check_lse(f64(lse[:, h:h + 1])[:, :, rows], lse_ref, TOL_LSE_BF16)
         check_close(f64(o[:, h:h + 1])[:, :, rows], o_ref, TOL_O_BF16)
-        tail = np.arange(w.N - 256, w.N)
-        dq_t, dk_t, dv_t = A.attn_bwd(qh, kh, vh, doh, 0, 0, True, rows=tail)
-        assert rel_fro(f64(dq[:, h:h + 1])[:, :, tail], dq_t) <= TOL_GRAD_REL
-        assert rel_fro(f64(dk[:, h:h + 1])[:, :, tail], dk_t[:, :, tail]) <= TOL_GRAD_REL
-        assert rel_fro(f64(dv[:, h:h + 1])[:, :, tail], dv_t[:, :, tail]) <= TOL_GRAD_REL
-        dq_s, _, _ = A.attn_bwd(qh, kh, vh, doh, 0, 0, True, rows=rows[rows < w.N - 256])
-        assert rel_fro(f64(dq[:, h:h + 1])[:, :, rows[rows < w.N - 256]], dq_s) <= TOL_GRAD_REL
+        # the last 2048 key rows are seen only by the last 2048 query rows, so
+        # the oracle over those rows gives their dK / dV exactly: 16 key
+        # tiles and 16 query tiles compared tile by tile
+        tail = np.arange(w.N - 2048, w.N)
+        dq_t, dk_t, dv_t = oracle_bwd_rows(qh, kh, vh, doh, 0, 0, True, tail)
+        for name, g, r in (("dQ", f64(dq[:, h:h + 1])[:, :, tail], dq_t),
+                           ("dK", f64(dk[:, h:h + 1])[:, :, tail], dk_t[:, :, tail]),
+                           ("dV", f64(dv[:, h:h + 1])[:, :, tail], dv_t[:, :, tail])):
+            assert rel_fro(g, r) <= TOL_GRAD_REL, name
+            check_tiles(g, r, name)
+        dq_s, _, _ = A.attn_bwd(qh, kh, vh, doh, 0, 0, True, rows=rows[rows < w.N - 2048])
+        assert rel_fro(f64(dq[:, h:h + 1])[:, :, rows[rows < w.N - 2048]], dq_s) <= TOL_GRAD_REL
     check_identities(q, k, v, o, d_o, dq, dk, dv, heads=range(0, 32, 3))
 
 
@@ -133,6 +139,17 @@ def test_noncausal_64k_heavy_tailed_scores():
     for b in range(2):
         check_identities(q[b:b + 1], k[b:b + 1], v[b:b + 1], o[b:b + 1], d_o[b:b + 1],
                          dq[b:b + 1], dk[b:b + 1], dv[b:b + 1], heads=(0, 5, 15), causal=False)
+    # one whole (b, h) against the oracle over all 65,536 query rows: dK and
+    # dV element by element and tile by tile, where the heavy key rows
+    # (scores up to ~180) sit among the rest
+    b, h = 1, 15
+    qh, kh, vh, doh = (f64(t[b:b + 1, h:h + 1]) for t in (q, k, v, d_o))
+    _, dk_r, dv_r = oracle_bwd_rows(qh, kh, vh, doh, 0, 0, False, np.arange(w.N))
+    for name, g, r in (("dK", f64(dk[b:b + 1, h:h + 1]), dk_r), ("dV", f64(dv[b:b + 1, h:h + 1]), dv_r)):
+        assert rel_fro(g, r) <= TOL_GRAD_REL, name
+        check_tiles(g, r, name)
+    heavy = x["heavy_rows"][b, h].cpu().numpy()
+    assert rel_fro(f64(dk[b:b + 1, h:h + 1])[:, :, heavy], dk_r[:, :, heavy]) <= TOL_GRAD_REL
 
 
 def test_decode_gqa_1m_full_size():

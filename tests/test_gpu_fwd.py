@@ -6,7 +6,7 @@ import torch
 
 from oracle import attention as A
 import long_sequence_exact_gb300 as lsx
-from long_sequence_exact_gb300.inputs import random_tensor
+from long_sequence_exact_gb300.inputs import WORKLOADS, make_inputs, random_tensor
 from helpers import TOL_LSE_BF16, TOL_O_BF16, check_close, check_lse, f64
 
 pytestmark = pytest.mark.gpu
@@ -115,3 +115,32 @@ def test_v_layouts_give_the_same_result():
     b = lsx.chunk_fwd(q, k, v, 200, 0, True, out_dtype=torch.float32, use_workspace=False)
     assert float((a[0] - b[0]).abs().max()) <= 1e-5
     assert float((a[1] - b[1]).abs().max()) <= 1e-5
+
+
+@pytest.mark.parametrize("partial_dtype", [torch.float32, torch.bfloat16])
+def test_heavy_tailed_d64_chunk_partials_merged(partial_dtype):
+    # The non-causal d = 64 workload's values at N = 4096, computed as 4 x 4
+    # chunk pairs: each query chunk visits its key chunks (own first, then
+    # the rest), and each new partial is merged into the running one by the
+    # forward's fused LSE merge.  Heavy keys (x 8) land in some chunks only,
+    # so the running maximum jumps by tens of units between partials: the
+    # merge weights span e^-100 .. 1.
+    w = WORKLOADS["noncausal_64k_heavytail"].with_(B=1, Hq=2, Hkv=2, N=4096)
+    x = make_inputs(w, device=DEV, with_grad=False)
+    q, k, v = x["q"], x["k"], x["v"]
+    c, nc = 1024, 4
+    o = torch.empty(q.shape, dtype=partial_dtype, device=DEV)
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device=DEV)
+    for qc in range(nc):
+        qs = slice(qc * c, (qc + 1) * c)
+        order = [qc] + [kc for kc in range(nc) if kc != qc]
+        for step, kc in enumerate(order):
+            ks = slice(kc * c, (kc + 1) * c)
+            lsx.chunk_fwd(q[:, :, qs], k[:, :, ks], v[:, :, ks], qc * c, kc * c, False,
+                          out=o[:, :, qs], lse=lse[:, :, qs], accumulate=step > 0)
+    torch.cuda.synchronize()
+    assert lsx.sync_status() == 0
+    o_ref, lse_ref = A.attn_fwd(f64(q), f64(k), f64(v), 0, 0, False)
+    assert np.max(lse_ref) > 100.0
+    check_lse(f64(lse), lse_ref, TOL_LSE_BF16)
+    check_close(f64(o), o_ref, TOL_O_BF16)

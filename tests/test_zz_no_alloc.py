@@ -17,7 +17,7 @@ import torch
 import long_sequence_exact_gb300 as lsx
 from long_sequence_exact_gb300 import _lib
 from long_sequence_exact_gb300.inputs import random_tensor
-from helpers import TOL_FP32, TOL_GRAD_REL, f64, rel_fro
+from helpers import TOL_FP32, TOL_GRAD_REL, check_tiles, f64, oracle_bwd_rows, rel_fro
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -72,6 +72,44 @@ def test_noalloc_matches_workspace_backward_on_consecutive_calls():
                     assert np.max(np.abs(gg - rr)) <= TOL_FP32
                 else:
                     assert rel_fro(gg, rr) <= TOL_GRAD_REL
+
+
+@pytest.mark.parametrize("grad_dtype", [torch.bfloat16, torch.float32])
+def test_noalloc_delta_only_branch_matches_oracle(grad_dtype):
+    # 65,536 query rows at d = 128: the row sums fit the fixed array (256 KiB)
+    # but the fp32 dQ accumulator and the operand copies (32 MiB) do not, so
+    # the call runs the backward without them: the two owner kernels for a
+    # bf16 dq, the fused kernel adding straight into an f32 dq.  Two calls
+    # in a row (different inputs), each against the oracle over every row
+    # and against the workspace entry point given the same minimum size.
+    lib = _lib.load()
+    b, hq, hkv, n, d = 1, 4, 2, 16384, 128
+    q0 = torch.empty((b, hq, n, d), dtype=torch.bfloat16, device=DEV)
+    k0 = torch.empty((b, hkv, n, d), dtype=torch.bfloat16, device=DEV)
+    vq, vk = _lib.view(q0), _lib.view(k0)
+    cap = lib.attn_chunk_bwd_noalloc_max_bytes()
+    assert lib.attn_chunk_bwd_min_workspace_size(ctypes.byref(vq), ctypes.byref(vk)) <= cap
+    assert lib.attn_chunk_bwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk)) > cap
+    for rep in range(2):
+        seed = 900 + 10 * rep
+        q = random_tensor((b, hq, n, d), seed, 0.5, device=DEV)
+        k = random_tensor((b, hkv, n, d), seed + 1, 0.5, device=DEV)
+        v = random_tensor((b, hkv, n, d), seed + 2, device=DEV)
+        d_o = random_tensor((b, hq, n, d), seed + 3, device=DEV)
+        o, lse = lsx.chunk_fwd(q, k, v, 0, 0, True)
+        got = _noalloc(q, k, v, o, lse, d_o, 0, 0, True, grad_dtype)
+        ws = lsx.chunk_bwd(q, k, v, o, lse, d_o, 0, 0, True, grad_dtype=grad_dtype,
+                           use_copies=False)
+        torch.cuda.synchronize()
+        assert lsx.sync_status() == 0
+        ref = oracle_bwd_rows(f64(q), f64(k), f64(v), f64(d_o), 0, 0, True, np.arange(n))
+        for name, g, w_, r in zip(("dQ", "dK", "dV"), got, ws, ref):
+            gg = f64(g)
+            assert not np.any(np.isnan(gg)), name
+            assert rel_fro(gg, r) <= TOL_GRAD_REL, name
+            check_tiles(gg, r, name)
+            # same kernels as the workspace call; dQ's fp32 adds land in run order
+            assert rel_fro(gg, f64(w_)) <= (2e-3 if name == "dQ" else 1e-6), name
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
