@@ -191,25 +191,77 @@ __device__ __forceinline__ void ld_two(uint32_t ta, uint32_t tb, uint32_t (&a)[3
 
 // P^T and dS^T of one grad thread's 32 scores when the score products
 // already hold S - LSE/scale and dP - delta; with kMask, the query columns
-// c < cmin (not yet visible to this key) get P = 0.
+// c < cmin (not yet visible to this key) get P = 0.  Formed in two halves,
+// so that P^T can be computed as soon as S^T is in, while dP^T is still
+// being computed: P of the 32 scores (kept in fp32 for dS, and packed to
+// bf16 for the dV product) ...
 template <bool kMask>
-__device__ __forceinline__ void grad_rows_rs(const uint32_t (&us)[32], const uint32_t (&ud)[32],
-                                             float2 sc2, int cmin, uint32_t (&pk)[16],
-                                             uint32_t (&dk)[16]) {
+__device__ __forceinline__ void p_rows_rs(const uint32_t (&us)[32], float2 sc2, int cmin,
+                                          float (&pr)[32], uint32_t (&pk)[16]) {
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
     const int c0 = 2 * e;
     const float2 arg = __fmul2_rn(
         make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2);
-    float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
+    float2 v = make_float2(ex2(arg.x), ex2(arg.y));
     if (kMask) {
-      if (c0 < cmin) pr.x = 0.f;
-      if (c0 + 1 < cmin) pr.y = 0.f;
+      if (c0 < cmin) v.x = 0.f;
+      if (c0 + 1 < cmin) v.y = 0.f;
     }
-    const float2 ds =
-        __fmul2_rn(pr, make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])));
-    pk[e] = pack_bf16(pr.x, pr.y);
+    pr[c0] = v.x;
+    pr[c0 + 1] = v.y;
+    pk[e] = pack_bf16(v.x, v.y);
+  }
+}
+// ... and dS^T = P^T o (dP^T - delta) once dP^T is in.
+__device__ __forceinline__ void ds_rows_rs(const float (&pr)[32], const uint32_t (&ud)[32],
+                                           uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float2 ds = __fmul2_rn(make_float2(pr[2 * e], pr[2 * e + 1]),
+                                 make_float2(__uint_as_float(ud[2 * e]),
+                                             __uint_as_float(ud[2 * e + 1])));
     dk[e] = pack_bf16(ds.x, ds.y);
+  }
+}
+// Without the statistics on the tensor cores: LSE (log2 units) and delta of
+// the 32 query columns come from shared memory.
+__device__ __forceinline__ void p_rows_st(const uint32_t (&us)[32], float2 sc2,
+                                          const float4* l2v, int cmin, float (&pr)[32],
+                                          uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 l4 = l2v[e4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int e = e4 * 2 + hh;
+      const int c0 = 2 * e;
+      const float2 nl = hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+      const float2 arg = __ffma2_rn(
+          make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
+      float2 v = make_float2(ex2(arg.x), ex2(arg.y));
+      if (c0 < cmin) v.x = 0.f;
+      if (c0 + 1 < cmin) v.y = 0.f;
+      pr[c0] = v.x;
+      pr[c0 + 1] = v.y;
+      pk[e] = pack_bf16(v.x, v.y);
+    }
+  }
+}
+__device__ __forceinline__ void ds_rows_st(const float (&pr)[32], const uint32_t (&ud)[32],
+                                           const float4* dlv, uint32_t (&dk)[16]) {
+#pragma unroll
+  for (int e4 = 0; e4 < 8; ++e4) {
+    const float4 d4 = dlv[e4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int e = e4 * 2 + hh;
+      const float2 nd = hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+      const float2 dpm = __fadd2_rn(
+          make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
+      const float2 ds = __fmul2_rn(make_float2(pr[2 * e], pr[2 * e + 1]), dpm);
+      dk[e] = pack_bf16(ds.x, ds.y);
+    }
   }
 }
 
@@ -254,7 +306,7 @@ struct DkdvSmem {
   uint64_t kv_full, kv_empty, final_bar, ones_full;
   uint64_t q_full[2], q_empty[2], o_full[2], o_empty[2];  // Q_i (+ statistics), dO_i slots
   uint64_t lse_full[2], lse_empty[2];
-  uint64_t s_full, p_full, dkv_done;
+  uint64_t s_ready, s_full, p_full, dkv_done;  // S^T in; S^T and dP^T in; P^T, dS^T out
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
   uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
   uint64_t stage_free[2];  // D = 64 with acc_tma: the dS^T tile's staged dQ has been read
@@ -374,6 +426,7 @@ __global__ void __launch_bounds__(640, 1)
       mbar_init(&sm.lse_full[s], 32);
       mbar_init(&sm.lse_empty[s], 512);
     }
+    mbar_init(&sm.s_ready, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.p_full, 512);
     mbar_init(&sm.dkv_done, 1);
@@ -503,6 +556,7 @@ __global__ void __launch_bounds__(640, 1)
             const uint64_t st = sdesc_interleave(smem_addr(sm.rs[qs]), 0, 128);
             mma_rows_by_rows<D>(tmem + 0, k_addr, q_addr, kIdS);
             if constexpr (kRS) mma_ss(tmem + 0, sel_c, st, kIdS, 1u);
+            mma_commit(&sm.s_ready);
             if (kQ128 && dq_pending) {  // dP^T reuses the columns of the last dQ^T
               if (!mbar_wait(&sm.dq_drained, dr_phase, guard)) { ok = false; break; }
               dr_phase ^= 1;
@@ -571,6 +625,7 @@ __global__ void __launch_bounds__(640, 1)
                 const uint64_t nst = sdesc_interleave(smem_addr(sm.rs[ns]), 0, 128);
                 mma_rows_by_rows<D>(tmem + 0, k_addr, smem_addr(sm.q[ns]), kIdS);
                 if constexpr (kRS) mma_ss(tmem + 0, sel_c, nst, kIdS, 1u);
+                mma_commit(&sm.s_ready);
                 if (!mbar_wait(&sm.o_full[ns], nph, guard)) { ok = false; break; }
                 tc_fence_after();
                 mma_rows_by_rows<D>(tmem + 128, v_addr, smem_addr(sm.d_o[ns]), kIdS);
@@ -596,7 +651,6 @@ __global__ void __launch_bounds__(640, 1)
               ++n_dq;
             }
           }
-          mma_commit(&sm.dkv_done);
           if constexpr (!kQ128 && !kQ64) {  // (kQ128: the reducer frees them; kQ64: above)
             mma_commit(&sm.q_empty[qs]);
             mma_commit(&sm.o_empty[qs]);
@@ -604,6 +658,9 @@ __global__ void __launch_bounds__(640, 1)
           if (++qs == kQoStages) { qs = 0; qph ^= 1; }
         }
         if (!ok) break;
+        // dK and dV are complete for the epilogue: one commit per item (the
+        // grad warps wait for its phase once per item)
+        if (x.n_i > 0) mma_commit(&sm.dkv_done);
         mma_commit(&sm.kv_empty);
       }
       if (issued) {
@@ -701,7 +758,7 @@ __global__ void __launch_bounds__(640, 1)
     const uint32_t tS = tmem + lane_base + 32 * qtr;        // S^T / P^T
     const uint32_t tP = tmem + lane_base + 128 + 32 * qtr;  // dP^T / dS^T
     uint32_t ls = 0, lph = 0, s_phase = 0, dq_phase = 0, gs = 0;
-    uint32_t d_count = 0;
+    uint32_t e_count = 0;  // items whose dK / dV have been read out
     const float sl2 = p.scale_log2;
     const float2 sc2 = make_float2(sl2, sl2);
     // D = 64 fused dQ: steps issued so far and the last step's (b, h, i);
@@ -760,12 +817,10 @@ __global__ void __launch_bounds__(640, 1)
       for (int64_t s = 0; s < x.n_i; ++s) {
         int64_t h, i;
         dkdv_step(p, x, s, h, i);
-        if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
-        s_phase ^= 1;
+        // P^T as soon as S^T is in (dP^T may still be in the tensor pipe)
+        if (!mbar_wait(&sm.s_ready, s_phase, guard)) { ok = false; break; }
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
         tc_fence_after();
-        uint32_t us[32], ud[32];
-        ld_two(tS, tP, us, ud);
         // query columns c (of this quarter) with q_off + 128 i + 32 qtr + c
         // >= key_abs are visible
         int cmin = 0;
@@ -775,44 +830,42 @@ __global__ void __launch_bounds__(640, 1)
         }
         const float4* l2v = reinterpret_cast<const float4*>(&sm.lse2[ls][32 * qtr]);
         const float4* dlv = reinterpret_cast<const float4*>(&sm.delta[ls][32 * qtr]);
+        float pr[32];
         uint32_t pk[16], dk[16];
-        if constexpr (kRS) {
-          // the scores already hold S - LSE/scale and dP - delta; only
-          // tiles that straddle the diagonal for this warp need the mask
-          const bool need_mask =
-              p.causal && p.kv_off + x.j * 128 + quad * 32 + 31 > p.q_off + i * 128 + 32 * qtr;
-          if (need_mask)
-            grad_rows_rs<true>(us, ud, sc2, cmin, pk, dk);
-          else
-            grad_rows_rs<false>(us, ud, sc2, cmin, pk, dk);
-          tmem_st16(tS, pk);
-          tmem_st16(tP, dk);
-        } else {
-          constexpr int cc = 0;
-#pragma unroll
-          for (int e4 = 0; e4 < 8; ++e4) {
-            const float4 l4 = l2v[cc * 8 + e4];
-            const float4 d4 = dlv[cc * 8 + e4];
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const int e = e4 * 2 + hh;  // pair index within the chunk
-              const int c0 = cc * 32 + 2 * e;
-              const float2 nl = hh ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
-              const float2 nd = hh ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
-              const float2 arg = __ffma2_rn(
-                  make_float2(__uint_as_float(us[2 * e]), __uint_as_float(us[2 * e + 1])), sc2, nl);
-              float2 pr = make_float2(ex2(arg.x), ex2(arg.y));
-              if (c0 < cmin) pr.x = 0.f;
-              if (c0 + 1 < cmin) pr.y = 0.f;
-              const float2 dpm = __fadd2_rn(
-                  make_float2(__uint_as_float(ud[2 * e]), __uint_as_float(ud[2 * e + 1])), nd);
-              const float2 ds = __fmul2_rn(pr, dpm);
-              pk[e] = pack_bf16(pr.x, pr.y);
-              dk[e] = pack_bf16(ds.x, ds.y);
-            }
+        {
+          uint32_t us[32];
+          tmem_ld32(tS, us);
+          tmem_ld_wait32(us);
+          if constexpr (kRS) {
+            // the scores already hold S - LSE/scale; only tiles that straddle
+            // the diagonal for this warp need the mask
+            const bool need_mask =
+                p.causal && p.kv_off + x.j * 128 + quad * 32 + 31 > p.q_off + i * 128 + 32 * qtr;
+            if (need_mask)
+              p_rows_rs<true>(us, sc2, cmin, pr, pk);
+            else
+              p_rows_rs<false>(us, sc2, cmin, pr, pk);
+          } else {
+            p_rows_st(us, sc2, l2v, cmin, pr, pk);
           }
-          tmem_st16(tS + cc * 16, pk);
-          tmem_st16(tP + cc * 16, dk);
+        }
+        tmem_st16(tS, pk);
+        tmem_st_wait();
+        // dS^T once dP^T is in
+        if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
+        s_phase ^= 1;
+        tc_fence_after();
+        {
+          uint32_t ud[32];
+          tmem_ld32(tP, ud);
+          tmem_ld_wait32(ud);
+          if constexpr (kRS)
+            ds_rows_rs(pr, ud, dk);
+          else
+            ds_rows_st(pr, ud, dlv, dk);
+        }
+        tmem_st16(tP, dk);
+        if constexpr (!kRS) {
           mbar_arrive(&sm.lse_empty[ls]);
           if (++ls == 2) { ls = 0; lph ^= 1; }
         }
@@ -837,7 +890,6 @@ __global__ void __launch_bounds__(640, 1)
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&sm.p_full);
-        ++d_count;
         if constexpr (kQ64) {
           if (n_g >= 1 && !drain64(n_g - 1, pb, ph, pi)) { ok = false; break; }
           pb = x.b; ph = h; pi = i;
@@ -846,23 +898,20 @@ __global__ void __launch_bounds__(640, 1)
         if constexpr (kQ128) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle,
           // the layout a TMA load of such a tile produces) into the slot of
-          // dO_i, once the dV product has finished reading it
-          // (the packed pairs are read back from TMEM rather than kept live
-          // in registers across the wait)
+          // dO_i, once the dV product has finished reading it (the packed
+          // pairs stay in registers across the wait: reading them back from
+          // TMEM would queue behind the dK product's accesses there)
           if (!mbar_wait(&sm.dv_done, dq_phase, guard)) { ok = false; break; }
           {
-            uint32_t w[16];
-            tmem_ld16_sync(tP, w);
             uint8_t* line = reinterpret_cast<uint8_t*>(sm.d_o[gs]) + (qtr >> 1) * 16384 + row * 128;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
               const int ch = (qtr & 1) * 4 + c4;  // 16-byte chunk (8 queries) in the line
               *reinterpret_cast<uint4*>(line + ((ch ^ (row & 7)) << 4)) =
-                  make_uint4(w[4 * c4], w[4 * c4 + 1], w[4 * c4 + 2], w[4 * c4 + 3]);
+                  make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
             }
           }
           fence_proxy_async_smem();
-          tc_fence_before();  // the TMEM read above precedes dQ^T's writes there
           mbar_arrive(&sm.ds_full);
           const uint32_t gs_prev = gs;
           if (++gs == 2) gs = 0;
@@ -908,7 +957,8 @@ __global__ void __launch_bounds__(640, 1)
       if (!ok) { grad_ok = false; break; }
       // epilogue: half 0 writes dV, half 1 writes dK (times scale)
       if (x.n_i > 0) {
-        if (!mbar_wait(&sm.dkv_done, (d_count - 1) & 1, guard)) { grad_ok = false; break; }
+        if (!mbar_wait(&sm.dkv_done, e_count & 1, guard)) { grad_ok = false; break; }
+        ++e_count;
         tc_fence_after();
       }
       const int64_t krow = x.j * 128 + row;
