@@ -632,15 +632,18 @@ __global__ void __launch_bounds__(640, 1)
                 if constexpr (kRS) mma_ss(tmem + 128, sel_d, nst, kIdS, 1u);
                 mma_commit(&sm.s_full);
               }
-              // dQ_i = dS K_j: A = dS^T's [key][query] tile and B = K_j's
-              // [key][d] tile, both MN-major; into the region of dQ_{i-2},
-              // once the grad warps have read that
+              // dQ_i = dS K_j: A = dS^T's [key][query] tile (written by the
+              // grad warps after p_full, ds_full) and B = K_j's [key][d] tile,
+              // both MN-major; into the region of dQ_{i-2}, once the grad
+              // warps have read that
               const int buf = static_cast<int>(n_dq & 1);
               if (n_dq >= 2) {
                 if (!mbar_wait(&sm.dq_free[buf], static_cast<uint32_t>((n_dq - 2) >> 1) & 1u,
                                guard)) { ok = false; break; }
-                tc_fence_after();
               }
+              if (!mbar_wait(&sm.ds_full, ds_phase, guard)) { ok = false; break; }
+              ds_phase ^= 1;
+              tc_fence_after();
               const uint64_t da0 = sdesc_sw128(smem_addr(sm.ds[buf]), 128 * 128, 1024);
               const uint64_t kb0 = sdesc_sw128(k_addr, 128 * 128, 1024);
 #pragma unroll
@@ -869,15 +872,21 @@ __global__ void __launch_bounds__(640, 1)
           mbar_arrive(&sm.lse_empty[ls]);
           if (++ls == 2) { ls = 0; lph ^= 1; }
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
         if constexpr (kQ64) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle)
-          // into its own tile; the dQ product that last read it (two steps
-          // back) completed before this warp's previous drain.  With acc_tma
-          // the tile has held that step's staged dQ since: wait (as late as
-          // possible) until the reducer has read it.
+          // into its own tile, after P^T and dS^T have been published in
+          // TMEM: only dQ_i, which the MMA thread issues after the next
+          // step's score products, reads the tile (ds_full), so these writes
+          // stay off the path to dV / dK.  The dQ product that last read the
+          // tile (two steps back) completed before this warp's previous
+          // drain.  With acc_tma the tile has held that step's staged dQ
+          // since: wait until the reducer has read it.
           if (p.acc_tma && n_g >= 2 &&
               !mbar_wait(&sm.stage_free[n_g & 1], static_cast<uint32_t>((n_g - 2) >> 1) & 1u,
-                         guard)) { tmem_st_wait(); ok = false; break; }
+                         guard)) { ok = false; break; }
           uint8_t* line = reinterpret_cast<uint8_t*>(sm.ds[n_g & 1]) + (qtr >> 1) * 16384 + row * 128;
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
@@ -886,11 +895,7 @@ __global__ void __launch_bounds__(640, 1)
                 make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
           }
           fence_proxy_async_smem();
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&sm.p_full);
-        if constexpr (kQ64) {
+          mbar_arrive(&sm.ds_full);
           if (n_g >= 1 && !drain64(n_g - 1, pb, ph, pi)) { ok = false; break; }
           pb = x.b; ph = h; pi = i;
           ++n_g;
