@@ -304,11 +304,13 @@ struct DkdvSmem {
   float lse2[2][128];             // LSE * log2(e); +inf for rows without keys
   float delta[2][128];
   uint64_t kv_full, kv_empty, final_bar, ones_full;
+  uint64_t final_dq;  // D = 64 fused: the dQ issuer's last products are complete
   uint64_t q_full[2], q_empty[2], o_full[2], o_empty[2];  // Q_i (+ statistics), dO_i slots
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_ready, s_full, p_full, dkv_done;  // S^T in; S^T and dP^T in; P^T, dS^T out
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
   uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
+  uint64_t ds_ready[2];  // D = 64: the dS^T tile of that parity has been written
   uint64_t stage_free[2];  // D = 64 with acc_tma: the dS^T tile's staged dQ has been read
   uint32_t tmem_base;
   int abort;
@@ -415,8 +417,11 @@ __global__ void __launch_bounds__(640, 1)
   if (threadIdx.x == 0) {
     sm.abort = 0;
     mbar_init(&sm.kv_full, 1);
-    mbar_init(&sm.kv_empty, 1);
+    // (D = 64 fused: K_j is also read by the dQ products of the second
+    // issuing thread, which releases the slot too)
+    mbar_init(&sm.kv_empty, kQ64 ? 2 : 1);
     mbar_init(&sm.final_bar, 1);
+    mbar_init(&sm.final_dq, 1);
     mbar_init(&sm.ones_full, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sm.q_full[s], 1);
@@ -436,6 +441,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.dq_drained, 512);
     mbar_init(&sm.stage_full, 512);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.ds_ready[b], 512);
       mbar_init(&sm.dq_done[b], 1);
       mbar_init(&sm.dq_free[b], 512);
       mbar_init(&sm.stage_free[b], 1);
@@ -525,8 +531,6 @@ __global__ void __launch_bounds__(640, 1)
       constexpr uint32_t kIdS = idesc_bf16_f32(128, 128, 0, 0);
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T = K^T dS^T
-      constexpr uint32_t kIdQ64 = idesc_bf16_f32(128, 64, 1, 1);  // dQ = dS K (D = 64)
-      int64_t n_dq = 0;  // dQ products issued (D = 64)
       uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0, ds_phase = 0, dr_phase = 0;
       bool issued = false, dq_pending = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
@@ -613,10 +617,11 @@ __global__ void __launch_bounds__(640, 1)
               // Q_i and dO_i have been read for the last time (dK, dV)
               mma_commit(&sm.q_empty[qs]);
               mma_commit(&sm.o_empty[qs]);
-              // The next step's S^T and dP^T go ahead of this step's dQ: the
-              // last readers of their columns (P^T by dV, dS^T by dK) precede
-              // them in issue order, and dQ reads only dS^T's shared tile and
-              // K_j, so dQ runs while the grad warps work on the next scores.
+              // The next step's S^T and dP^T right away: the last readers of
+              // their columns (P^T by dV, dS^T by dK) precede them in issue
+              // order; this step's dQ, which reads only dS^T's shared tile and
+              // K_j, is issued by the second MMA thread and runs while the
+              // grad warps work on the next scores.
               if (s + 1 < x.n_i) {
                 const uint32_t ns = qs + 1 == kQoStages ? 0u : qs + 1;
                 const uint32_t nph = qs + 1 == kQoStages ? qph ^ 1u : qph;
@@ -632,26 +637,7 @@ __global__ void __launch_bounds__(640, 1)
                 if constexpr (kRS) mma_ss(tmem + 128, sel_d, nst, kIdS, 1u);
                 mma_commit(&sm.s_full);
               }
-              // dQ_i = dS K_j: A = dS^T's [key][query] tile (written by the
-              // grad warps after p_full, ds_full) and B = K_j's [key][d] tile,
-              // both MN-major; into the region of dQ_{i-2}, once the grad
-              // warps have read that
-              const int buf = static_cast<int>(n_dq & 1);
-              if (n_dq >= 2) {
-                if (!mbar_wait(&sm.dq_free[buf], static_cast<uint32_t>((n_dq - 2) >> 1) & 1u,
-                               guard)) { ok = false; break; }
-              }
-              if (!mbar_wait(&sm.ds_full, ds_phase, guard)) { ok = false; break; }
-              ds_phase ^= 1;
-              tc_fence_after();
-              const uint64_t da0 = sdesc_sw128(smem_addr(sm.ds[buf]), 128 * 128, 1024);
-              const uint64_t kb0 = sdesc_sw128(k_addr, 128 * 128, 1024);
-#pragma unroll
-              for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tmem + (buf ? 448u : 320u), da0 + mnmajor_step(kk), kb0 + mnmajor_step(kk),
-                       kIdQ64, kk > 0 ? 1u : 0u);
-              mma_commit(&sm.dq_done[buf]);
-              ++n_dq;
+              // (dQ_i = dS K_j is issued by the second MMA thread, warp 3)
             }
           }
           if constexpr (!kQ128 && !kQ64) {  // (kQ128: the reducer frees them; kQ64: above)
@@ -669,6 +655,62 @@ __global__ void __launch_bounds__(640, 1)
       if (issued) {
         mma_commit(&sm.final_bar);
         drain_wait(&sm.final_bar, 0, p.wait_ns);
+      }
+    } else if (kQ64 && warp == 3 && lane == 0) {
+      // --------------------------------- dQ issue (fused form, D = 64)
+      // A second MMA-issuing thread: at d = 64 one thread cannot issue the
+      // 34 products of a step as fast as the tensor pipe runs them.  dQ_i =
+      // dS K_j reads only dS^T's shared tile (ds_ready, written after the
+      // grad warps published P^T and dS^T) and the K_j tile, and writes its
+      // own TMEM region (alternately [320,384) and [448,512), once the grad
+      // warps have drained dQ_{i-2} from it), so its order relative to the
+      // first thread's products does not matter; its completion is tracked
+      // by its own commits (dq_done, and kv_empty: K_j's slot is free only
+      // when both threads' products of the item are complete).
+      constexpr uint32_t kIdQ64 = idesc_bf16_f32(128, 64, 1, 1);  // dQ = dS K
+      const uint32_t k_addr = smem_addr(sm.k);
+      uint32_t kv_phase = 0;
+      int64_t n_dq = 0;
+      bool issued = false;
+      for (int64_t r = 0;; ++r) {
+        const int64_t it = snake_item(c, r, G);
+        if (it >= p.n_items) break;
+        const DkdvItem x = dkdv_item(p, it);
+        if (!mbar_wait(&sm.kv_full, kv_phase, guard)) break;
+        kv_phase ^= 1;
+        bool ok = true;
+        for (int64_t s = 0; s < x.n_i; ++s) {
+          const int buf = static_cast<int>(n_dq & 1);
+          if (n_dq >= 2 &&
+              !mbar_wait(&sm.dq_free[buf], static_cast<uint32_t>((n_dq - 2) >> 1) & 1u, guard)) {
+            ok = false;
+            break;
+          }
+          // (one barrier per tile: the tile's next write, two steps on, waits
+          // for this product through the reducer, so a phase is never missed)
+          if (!mbar_wait(&sm.ds_ready[buf], static_cast<uint32_t>(n_dq >> 1) & 1u, guard)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          // A = dS^T's [key][query] tile and B = K_j's [key][d] tile, both
+          // MN-major
+          const uint64_t da0 = sdesc_sw128(smem_addr(sm.ds[buf]), 128 * 128, 1024);
+          const uint64_t kb0 = sdesc_sw128(k_addr, 128 * 128, 1024);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ss(tmem + (buf ? 448u : 320u), da0 + mnmajor_step(kk), kb0 + mnmajor_step(kk),
+                   kIdQ64, kk > 0 ? 1u : 0u);
+          mma_commit(&sm.dq_done[buf]);
+          ++n_dq;
+          issued = true;
+        }
+        if (!ok) break;
+        mma_commit(&sm.kv_empty);
+      }
+      if (issued) {
+        mma_commit(&sm.final_dq);
+        drain_wait(&sm.final_dq, 0, p.wait_ns);
       }
     } else if (kQ64 && p.acc_tma && warp == 2 && lane == 0) {
       // ------------------------------------- dQ reducer (fused form, D = 64)
@@ -878,12 +920,12 @@ __global__ void __launch_bounds__(640, 1)
         if constexpr (kQ64) {
           // dS^T as bf16 [key][query] (two 64-query boxes, 128-byte swizzle)
           // into its own tile, after P^T and dS^T have been published in
-          // TMEM: only dQ_i, which the MMA thread issues after the next
-          // step's score products, reads the tile (ds_full), so these writes
-          // stay off the path to dV / dK.  The dQ product that last read the
-          // tile (two steps back) completed before this warp's previous
-          // drain.  With acc_tma the tile has held that step's staged dQ
-          // since: wait until the reducer has read it.
+          // TMEM: only dQ_i, which the second MMA thread issues, reads the
+          // tile (ds_ready), so these writes stay off the path to dV / dK.
+          // The dQ product that last read the tile (two steps back)
+          // completed before this warp's previous drain.  With acc_tma the
+          // tile has held that step's staged dQ since: wait until the
+          // reducer has read it.
           if (p.acc_tma && n_g >= 2 &&
               !mbar_wait(&sm.stage_free[n_g & 1], static_cast<uint32_t>((n_g - 2) >> 1) & 1u,
                          guard)) { ok = false; break; }
@@ -895,7 +937,7 @@ __global__ void __launch_bounds__(640, 1)
                 make_uint4(dk[4 * c4], dk[4 * c4 + 1], dk[4 * c4 + 2], dk[4 * c4 + 3]);
           }
           fence_proxy_async_smem();
-          mbar_arrive(&sm.ds_full);
+          mbar_arrive(&sm.ds_ready[n_g & 1]);
           if (n_g >= 1 && !drain64(n_g - 1, pb, ph, pi)) { ok = false; break; }
           pb = x.b; ph = h; pi = i;
           ++n_g;
