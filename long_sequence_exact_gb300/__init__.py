@@ -3,7 +3,9 @@
 The compute lives in ``liblsx.so`` (hand-written CUDA for sm_103a, C ABI in
 ``include/lsx.h``); ``attention`` is a thin ctypes binding with the same
 entry points.  Importing this package does not load the library; the first
-call does, and raises if it has not been built.
+call does, and raises if it has not been built.  ``ring`` runs the same calls
+across ranks (the ring of chunk pairs, and the cross-rank merge of decode
+partials) over torch.distributed.
 """
 
 from .attention import (  # noqa: F401
@@ -27,6 +29,7 @@ from .attention import (  # noqa: F401
     version,
 )
 from .autograd import ChunkedAttention, chunked_attention  # noqa: F401
+from . import ring  # noqa: F401
 
 __all__ = [
     "chunk_fwd", "chunk_bwd", "chunked_fwd", "chunked_bwd", "block_sparse_fwd",

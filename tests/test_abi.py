@@ -20,7 +20,8 @@ def lib():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     names = re.findall(r"^\s*(?:const\s+)?[\w\*\s]+?\b((?:attn|lsx)_\w+)\s*\(", text, flags=re.M)
     return sorted(set(names))

@@ -37,7 +37,7 @@ def _rank_main(rank, world, port, out):
 def test_two_ranks_report_the_slowest_rank_and_the_job_rate():
     world = 2
     port = _free_port()
-    manager = mp.Manager()
+    manager = mp.get_context("spawn").Manager()
     out = manager.dict()
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     expect_ms = 15.0
