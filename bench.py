@@ -53,12 +53,21 @@ KERNEL_SOURCES = {
 TRACE_KERNELS = {0: "fwd_tc", 1: "bwd_dkdv_tc", 2: "bwd_dq_tc", 12: "bwd_fused_tc"}
 
 
+def _code_only(text):
+    """Source text without comments and with whitespace runs collapsed, so
+    that editing a comment does not count as changing the kernel."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(name):
     import hashlib
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[name]:
-        with open(os.path.join(PKG, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(PKG, rel)) as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,47 +14,51 @@
 //    of the group) that sees it:
 //      S^T  = K Q_i^T     (SS, K-major x K-major)      TMEM [0,128)
 //      dP^T = V dO_i^T    (SS)                         TMEM [128,256)
-//      grad warps: P^T, dS^T -> bf16 back into TMEM (inside [0,128), [128,256))
+//      grad warps: P^T once S^T is in, dS^T once dP^T is in, each as bf16
+//      back into the first 16 columns of the warp's quarter of its tile
 //      dV  += P^T dO_i    (TS, dO_i MN-major)          TMEM [256,256+D)
 //      dK  += dS^T Q_i    (TS, Q_i MN-major)           TMEM [384,384+D)
-//    With kDq (D = 128) it also forms dQ: once dV has read dO_i for the
+//    With kDq and D = 128 it also forms dQ: once dV has read dO_i for the
 //    last time, the grad warps write dS^T into dO_i's shared-memory slot and
 //      dQ_i^T = K^T dS^T  (SS, both MN-major)          TMEM [128,256)
 //    which they read back (the next dP^T waits only for that), scale and
-//    stage as fp32 [query][d] rows in the now dead Q_i / dO_i slots; one
-//    thread of warp 2 adds the staged tile into the fp32 dQ accumulator
-//    with bulk TMA reduce-adds and frees the slots for the next loads once
-//    the TMA unit has read them.  dK and dV stay owned by one CTA each; dQ's
-//    summation order varies between runs.
+//    stage in the now dead Q_i / dO_i slots; one thread of warp 2 adds the
+//    staged tile into the fp32 dQ accumulator with TMA reduce-adds and frees
+//    the slots for the next loads once the TMA unit has read them.  dK and
+//    dV stay owned by one CTA each; dQ's summation order varies between
+//    runs.
 //    With kDq and D = 64, TMEM has room to spare and shared memory too:
 //      dQ_i = dS K        (SS, both MN-major)     TMEM [320,384) / [448,512)
-//    alternating between the two free 64-column regions, with dS^T in its
-//    own double-buffered shared tile written before P^T is published.  The
-//    MMA thread issues step i+1's S^T / dP^T ahead of dQ_i (dV and dK, the
-//    last readers of their columns, come first), so dQ_i runs under the
-//    grad warps' next step.  During step i+1 the grad warps read dQ_i back
-//    and stage it, scaled, in dS_i^T's spent tile as two swizzled [128
-//    queries][32 d] fp32 boxes; one thread of warp 2 adds them into the
-//    target with tensor-map reduce-adds and releases the tile for the dS^T
-//    of step i+2.  (Where the target takes no tensor map the grad warps add
-//    with 16-byte vector atomics instead.)
-//  * dq_kernel (the deterministic form of dQ), query-tile-major: a work item is one 128-row query tile; it
-//    walks every visible key tile:
+//    alternating between the two free 64-column regions, issued by a second
+//    MMA thread (warp 3) from dS^T's own double-buffered shared tile, which
+//    the grad warps write after publishing P^T and dS^T.  The first MMA
+//    thread issues step i+1's S^T / dP^T right after dV_i / dK_i (the last
+//    readers of their columns), so dQ_i runs under the grad warps' next
+//    step.  During step i+1 the grad warps read dQ_i back and stage it,
+//    scaled, in dS_i^T's spent tile as two swizzled [128 queries][32 d]
+//    fp32 boxes; one thread of warp 2 adds them into the target with
+//    tensor-map reduce-adds and releases the tile for the dS^T of step i+2.
+//    (Where the target takes no tensor map the grad warps add with 16-byte
+//    vector atomics instead.)
+//  * dq_kernel (the deterministic form of dQ), query-tile-major: a work item
+//    is one 128-row query tile; it walks every visible key tile:
 //      S  = Q K_j^T, dP = dO V_j^T (SS)                TMEM [0,128), [128,256)
 //      grad warps: dS -> bf16 into TMEM (inside [128,256))
 //      dQ += dS K_j       (TS, K_j MN-major)           TMEM [256,256+D)
-// Roles per CTA (384 threads): warp 0 loads (TMA), warp 1 owns TMEM and
-// issues the MMAs (lane 0), warps 4..11 compute P and dS and write the
-// outputs.  Grad warp g covers TMEM lanes 32 (g % 4) .. +31 and the half
-// g / 4 of the 128 columns; each half packs its bf16 result into the first
-// 32 columns of its own 64, so the two warps sharing a lane range never
-// touch each other's columns, and the TS MMAs address each 16-wide K step
-// of the bf16 operand at packed_col(kk).
-// MMA issue order: the next step's S/dP products are issued right after the
-// current dV/dK (dQ) products without waiting for them; one thread's
-// tcgen05.mma operations execute in issue order, so the bf16 operands read
-// by the earlier MMAs are consumed before the later MMAs overwrite them.
-// Work items are dealt longest-first in snake order.
+// Roles per CTA (640 threads): warp 0 loads (TMA), warp 1 owns TMEM and
+// issues the MMAs (lane 0; with fused dQ at D = 64, warp 3 issues the dQ
+// products), warp 2 (lane 0) adds the staged dQ into its target, and the 16
+// grad warps 4..19 compute P and dS and write the outputs.  Grad warp g
+// covers TMEM lanes 32 (g % 4) .. +31 and the quarter g / 4 of the 128
+// columns; each quarter packs its bf16 result into its own first 16
+// columns, so warps sharing a lane range never touch each other's columns,
+// and the TS MMAs address each 16-wide K step of the bf16 operand at
+// packed_col(kk).
+// MMA issue order: products of one thread execute in issue order, so a
+// product that overwrites TMEM columns is issued after the products that
+// read them (e.g. the next S^T after the dV that reads P^T); products of
+// the two issuing threads touch disjoint columns and are ordered by
+// barriers.  Work items are dealt longest-first in snake order.
 #include <cuda_bf16.h>
 #include <math.h>
 

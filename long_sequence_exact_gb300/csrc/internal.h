@@ -159,7 +159,8 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
 // tcgen05 tensor-core backward (bf16 inputs).  Unless the deterministic
 // mode is set, one kernel computes dK, dV and dQ (D = 128 or 64), adding each
 // key tile's dQ contribution into an fp32 accumulator: copies.dq_acc
-// (dense [B, Hq, Lq, D], zeroed and converted to dq by the launcher) or,
+// (at D = 128 transposed [B, Hq, 128, Np], at D = 64 dense [B, Hq, Lq, 64];
+// zeroed and converted to dq by the launcher) or,
 // when dq itself is f32, dq directly.  Otherwise two kernels own their
 // outputs: with copies.kt non-NULL, a key-contiguous copy of K is written
 // there first and the dQ product reads it K-major; with NULL the K tiles
