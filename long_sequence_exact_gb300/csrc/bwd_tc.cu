@@ -18,6 +18,8 @@
 //      back into the first 16 columns of the warp's quarter of its tile
 //      dV  += P^T dO_i    (TS, dO_i MN-major)          TMEM [256,256+D)
 //      dK  += dS^T Q_i    (TS, Q_i MN-major)           TMEM [384,384+D)
+//    dV is issued as soon as P^T is stored, so it runs while dS^T is
+//    formed; dK once dS^T is.
 //    With kDq and D = 128 it also forms dQ: once dV has read dO_i for the
 //    last time, the grad warps write dS^T into dO_i's shared-memory slot and
 //      dQ_i^T = K^T dS^T  (SS, both MN-major)          TMEM [128,256)
@@ -312,6 +314,7 @@ struct DkdvSmem {
   uint64_t q_full[2], q_empty[2], o_full[2], o_empty[2];  // Q_i (+ statistics), dO_i slots
   uint64_t lse_full[2], lse_empty[2];
   uint64_t s_ready, s_full, p_full, dkv_done;  // S^T in; S^T and dP^T in; P^T, dS^T out
+  uint64_t pt_full;  // P^T out (dV may start while dS^T is being formed)
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
   uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
   uint64_t ds_ready[2];  // D = 64: the dS^T tile of that parity has been written
@@ -438,6 +441,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.s_ready, 1);
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.p_full, 512);
+    mbar_init(&sm.pt_full, 512);
     mbar_init(&sm.dkv_done, 1);
     mbar_init(&sm.dv_done, 1);
     mbar_init(&sm.ds_full, 512);
@@ -576,22 +580,26 @@ __global__ void __launch_bounds__(640, 1)
             mma_commit(&sm.s_full);
             issued = true;
           }
-          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
-          p_phase ^= 1;
+          // dV += P^T dO_i as soon as P^T is in TMEM (pt_full): it runs while
+          // the grad warps form dS^T; dK waits for that (p_full)
+          if (!mbar_wait(&sm.pt_full, p_phase, guard)) { ok = false; break; }
           const uint32_t bq = q_addr, bo = o_addr;
           tc_fence_after();
+          const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
+          const uint32_t acc0 = s > 0 ? 1u : 0u;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG,
+                   kk > 0 ? 1u : acc0);
+          if constexpr (kQ128) mma_commit(&sm.dv_done);  // dO_i has been read for the last time
+          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
+          p_phase ^= 1;
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
+                   kk > 0 ? 1u : acc0);
           if constexpr (kQ128) {
-            const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
-            const uint32_t acc0 = s > 0 ? 1u : 0u;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG,
-                     kk > 0 ? 1u : acc0);
-            mma_commit(&sm.dv_done);  // dO_i has been read for the last time
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
-                     kk > 0 ? 1u : acc0);
             if (!mbar_wait(&sm.ds_full, ds_phase, guard)) { ok = false; break; }
             ds_phase ^= 1;
             tc_fence_after();
@@ -607,16 +615,6 @@ __global__ void __launch_bounds__(640, 1)
             mma_commit(&sm.dq_full);
             dq_pending = true;
           } else {
-            // (kQ64 runs the same dV / dK products, then dQ below)
-            const uint64_t bo0 = seq_b_base<D, false>(bo), bq0 = seq_b_base<D, false>(bq);
-            const uint32_t acc0 = s > 0 ? 1u : 0u;
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              const uint32_t acc = kk > 0 ? 1u : acc0;
-              mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG, acc);
-              mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk), kIdG,
-                     acc);
-            }
             if constexpr (kQ64) {
               // Q_i and dO_i have been read for the last time (dK, dV)
               mma_commit(&sm.q_empty[qs]);
@@ -900,6 +898,8 @@ __global__ void __launch_bounds__(640, 1)
         }
         tmem_st16(tS, pk);
         tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&sm.pt_full);
         // dS^T once dP^T is in
         if (!mbar_wait(&sm.s_full, s_phase, guard)) { ok = false; break; }
         s_phase ^= 1;
