@@ -334,20 +334,32 @@ __global__ void __launch_bounds__(384, 1)
     const int row = threadIdx.x - 128 * (1 + t);  // 0..127 == TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + lane_base + t * 128;
-    const uint32_t tO = tmem + lane_base + 256 + t * 128;
+    const uint32_t tO = tS + 256;
     uint32_t s_phase = 0;
     uint32_t pv_count = 0;
     const float sl2 = p.scale_log2;
-    for (int64_t r = 0;; ++r) {
-      const int64_t it = snake_item(c, r, G);
+    // The key-tile loop holds 128 scores in registers: keep little else live
+    // across it (the item is decoded again for the epilogue, the wait guard
+    // is rebuilt from the parameters at each wait, the grid position is
+    // re-read), so that none of it spills.
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+      return mbar_wait(bar, parity, WaitGuard{p.status, p.wait_ns, &sm.abort});
+    };
+    for (int r = 0;; ++r) {
+      const int64_t it = snake_item(blockIdx.x, r, gridDim.x);
       if (it >= p.n_items) break;
-      const Item x = decode_item(p, it);
-      const int64_t nkv = x.nkv[t];
-      const int64_t qr0 = (2 * x.pair + t) * 128;
+      int nkv;
+      int64_t pair;
+      {
+        const Item x = decode_item(p, it);
+        nkv = static_cast<int>(x.nkv[t]);
+        pair = x.pair;
+      }
+      const int64_t qr0 = (2 * pair + t) * 128;
       float m = kNegInf, l = 0.f;
       bool ok = true;
-      for (int64_t j = 0; j < nkv; ++j) {
-        if (!mbar_wait(&sm.s_full[t], s_phase, guard)) { ok = false; break; }
+      for (int j = 0; j < nkv; ++j) {
+        if (!wait(&sm.s_full[t], s_phase)) { ok = false; break; }
         s_phase ^= 1;
         tc_fence_after();
         float s[128];
@@ -370,10 +382,11 @@ __global__ void __launch_bounds__(384, 1)
             s[96 + i] = __uint_as_float(u3[i]);
           }
         }
-        const int64_t kb = key_tile(p, x, j) * 128;
+        const int64_t kb =
+            (p.pair_list == nullptr ? j : p.pair_list[pair * p.n_kb + j]) * int64_t{128};
         // a listed tile whose block this query tile does not have: all masked
         const bool blk_off =
-            p.bmask != nullptr && p.bmask[(2 * x.pair + t) * p.n_kb + kb / 128] == 0;
+            p.bmask != nullptr && p.bmask[(2 * pair + t) * p.n_kb + kb / 128] == 0;
         const bool need_mask =
             blk_off || (kb + 128 > p.Lk) || (p.causal && p.kv_off + kb + 127 > p.q_off + qr0);
         if (need_mask) {
@@ -404,7 +417,7 @@ __global__ void __launch_bounds__(384, 1)
           const bool need = m_new > m + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
             // O_t must hold the finished P_t V of the previous key tile
-            if (!mbar_wait(&sm.o_full[t], (pv_count - 1) & 1, guard)) { ok = false; break; }
+            if (!wait(&sm.o_full[t], (pv_count - 1) & 1)) { ok = false; break; }
             tc_fence_after();
             const float alpha = (m == kNegInf) ? 0.f : ex2(m - m_new);
 #pragma unroll
@@ -448,10 +461,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // --------------------------------------------------------- epilogue
+      const Item x = decode_item(p, it);
       const int64_t qrow = qr0 + row;
       const bool valid = qrow < p.Lq;
       if (nkv > 0) {
-        if (!mbar_wait(&sm.o_full[t], (pv_count - 1) & 1, guard)) break;
+        if (!wait(&sm.o_full[t], (pv_count - 1) & 1)) break;
         tc_fence_after();
       }
       const float inv = (l > 0.f) ? 1.f / l : 0.f;
