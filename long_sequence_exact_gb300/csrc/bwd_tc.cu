@@ -33,10 +33,11 @@
 //      dQ_i = dS K        (SS, both MN-major)     TMEM [320,384) / [448,512)
 //    alternating between the two free 64-column regions, issued by a second
 //    MMA thread (warp 3) from dS^T's own double-buffered shared tile, which
-//    the grad warps write after publishing P^T and dS^T.  The first MMA
-//    thread issues step i+1's S^T / dP^T right after dV_i / dK_i (the last
-//    readers of their columns), so dQ_i runs under the grad warps' next
-//    step.  During step i+1 the grad warps read dQ_i back and stage it,
+//    the grad warps write after publishing P^T and dS^T.  That thread also
+//    issues dK_i, in parallel with the first thread's dV_i; the first thread
+//    issues step i+1's S^T right after dV_i (the last reader of its
+//    columns) and its dP^T once dK_i has completed (dk_done), so dQ_i runs
+//    under the grad warps' next step.  During step i+1 the grad warps read dQ_i back and stage it,
 //    scaled, in dS_i^T's spent tile as two swizzled [128 queries][32 d]
 //    fp32 boxes; one thread of warp 2 adds them into the target with
 //    tensor-map reduce-adds and releases the tile for the dS^T of step i+2.
@@ -48,8 +49,8 @@
 //      grad warps: dS -> bf16 into TMEM (inside [128,256))
 //      dQ += dS K_j       (TS, K_j MN-major)           TMEM [256,256+D)
 // Roles per CTA (640 threads): warp 0 loads (TMA), warp 1 owns TMEM and
-// issues the MMAs (lane 0; with fused dQ at D = 64, warp 3 issues the dQ
-// products), warp 2 (lane 0) adds the staged dQ into its target, and the 16
+// issues the MMAs (lane 0; with fused dQ at D = 64, warp 3 issues the dK
+// and dQ products), warp 2 (lane 0) adds the staged dQ into its target, and the 16
 // grad warps 4..19 compute P and dS and write the outputs.  Grad warp g
 // covers TMEM lanes 32 (g % 4) .. +31 and the quarter g / 4 of the 128
 // columns; each quarter packs its bf16 result into its own first 16
@@ -318,6 +319,7 @@ struct DkdvSmem {
   uint64_t dv_done, ds_full, dq_full, dq_drained, stage_full;  // fused dQ, D = 128
   uint64_t dq_done[2], dq_free[2];                             // fused dQ, D = 64
   uint64_t ds_ready[2];  // D = 64: the dS^T tile of that parity has been written
+  uint64_t dk_done;      // D = 64 fused: this step's dK (second issuer) has completed
   uint64_t stage_free[2];  // D = 64 with acc_tma: the dS^T tile's staged dQ has been read
   uint32_t tmem_base;
   int abort;
@@ -344,12 +346,25 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
   return x;
 }
 
-// Query head and query tile of step s of a dK/dV item.
-__device__ __forceinline__ void dkdv_step(const BwdParams& p, const DkdvItem& x, int64_t s,
+// The steps of a dK/dV item in order: every query tile of the group's
+// first head, then of the next head.  A cursor advanced once per step (a
+// 64-bit division per step would cost each thread that walks the item a
+// few hundred cycles).
+struct DkdvCursor {
+  int64_t h, r;  // query head; position among the item's query tiles of a head
+};
+__device__ __forceinline__ DkdvCursor dkdv_first(const DkdvItem& x) {
+  return DkdvCursor{x.hk * x.group, 0};
+}
+// Query head and query tile of the cursor's step, then on to the next step.
+__device__ __forceinline__ void dkdv_take(const BwdParams& p, const DkdvItem& x, DkdvCursor& cur,
                                           int64_t& h, int64_t& i) {
-  h = x.hk * x.group + s / x.len;
-  const int64_t r = s % x.len;
-  i = p.col_list == nullptr ? x.i0 + r : p.col_list[x.j * p.n_qtiles + r];
+  h = cur.h;
+  i = p.col_list == nullptr ? x.i0 + cur.r : p.col_list[x.j * p.n_qtiles + cur.r];
+  if (++cur.r == x.len) {
+    cur.r = 0;
+    ++cur.h;
+  }
 }
 
 // Loads one 128-row tile as D/64 boxes of [128 rows][64 cols] (row-major
@@ -442,6 +457,7 @@ __global__ void __launch_bounds__(640, 1)
     mbar_init(&sm.s_full, 1);
     mbar_init(&sm.p_full, 512);
     mbar_init(&sm.pt_full, 512);
+    mbar_init(&sm.dk_done, 1);
     mbar_init(&sm.dkv_done, 1);
     mbar_init(&sm.dv_done, 1);
     mbar_init(&sm.ds_full, 512);
@@ -494,9 +510,10 @@ __global__ void __launch_bounds__(640, 1)
           load_tile<D, false>(sm.v, &tm_v, &sm.kv_full, x.j * 128, x.hk, x.b);
         }
         bool ok = true;
+        DkdvCursor cur = dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s) {
           int64_t h, i;
-          dkdv_step(p, x, s, h, i);
+          dkdv_take(p, x, cur, h, i);
           // Q_i, dO_i (B operands of S^T, dP^T and, read MN-major, of dK, dV);
           // the two slots are freed separately (the fused form frees Q_i's
           // first) and S^T waits only for Q_i
@@ -540,6 +557,7 @@ __global__ void __launch_bounds__(640, 1)
       constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);
       constexpr uint32_t kIdQ = idesc_bf16_f32(128, 128, 1, 1);  // dQ^T = K^T dS^T
       uint32_t qs = 0, qph = 0, kv_phase = 0, p_phase = 0, ds_phase = 0, dr_phase = 0;
+      uint32_t dk_phase = 0;
       bool issued = false, dq_pending = false;
       const uint32_t k_addr = smem_addr(sm.k), v_addr = smem_addr(sm.v);
       // selector and statistics tiles: 16 core matrices of 8 rows x 16 bytes
@@ -592,6 +610,40 @@ __global__ void __launch_bounds__(640, 1)
             mma_ts(tmem + 256, tmem + packed_col(kk), bo0 + seq_b_step<D, false>(kk), kIdG,
                    kk > 0 ? 1u : acc0);
           if constexpr (kQ128) mma_commit(&sm.dv_done);  // dO_i has been read for the last time
+          if constexpr (kQ64) {
+            // dK_i is issued by the second MMA thread (warp 3), in parallel
+            // with dV_i here.  dO_i has been read for the last time (dP^T,
+            // dV); Q_i's slot is released by that thread after dK_i.
+            p_phase ^= 1;
+            mma_commit(&sm.o_empty[qs]);
+            // The next S^T right away: dV_i, the last reader of its columns
+            // (P^T), precedes it in this thread's issue order.  The next dP^T
+            // overwrites dS^T_i, which dK_i reads: it waits for dK_i.
+            const bool next = s + 1 < x.n_i;
+            const uint32_t ns = qs + 1 == kQoStages ? 0u : qs + 1;
+            const uint32_t nph = qs + 1 == kQoStages ? qph ^ 1u : qph;
+            if (next) {
+              if (!mbar_wait(&sm.q_full[ns], nph, guard)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t nst = sdesc_interleave(smem_addr(sm.rs[ns]), 0, 128);
+              mma_rows_by_rows<D>(tmem + 0, k_addr, smem_addr(sm.q[ns]), kIdS);
+              if constexpr (kRS) mma_ss(tmem + 0, sel_c, nst, kIdS, 1u);
+              mma_commit(&sm.s_ready);
+            }
+            if (!mbar_wait(&sm.dk_done, dk_phase, guard)) { ok = false; break; }
+            dk_phase ^= 1;
+            tc_fence_after();
+            if (next) {
+              if (!mbar_wait(&sm.o_full[ns], nph, guard)) { ok = false; break; }
+              tc_fence_after();
+              const uint64_t nst = sdesc_interleave(smem_addr(sm.rs[ns]), 0, 128);
+              mma_rows_by_rows<D>(tmem + 128, v_addr, smem_addr(sm.d_o[ns]), kIdS);
+              if constexpr (kRS) mma_ss(tmem + 128, sel_d, nst, kIdS, 1u);
+              mma_commit(&sm.s_full);
+            }
+            if (++qs == kQoStages) { qs = 0; qph ^= 1; }
+            continue;
+          }
           if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
           p_phase ^= 1;
           tc_fence_after();
@@ -614,33 +666,6 @@ __global__ void __launch_bounds__(640, 1)
                      kk > 0 ? 1u : 0u);
             mma_commit(&sm.dq_full);
             dq_pending = true;
-          } else {
-            if constexpr (kQ64) {
-              // Q_i and dO_i have been read for the last time (dK, dV)
-              mma_commit(&sm.q_empty[qs]);
-              mma_commit(&sm.o_empty[qs]);
-              // The next step's S^T and dP^T right away: the last readers of
-              // their columns (P^T by dV, dS^T by dK) precede them in issue
-              // order; this step's dQ, which reads only dS^T's shared tile and
-              // K_j, is issued by the second MMA thread and runs while the
-              // grad warps work on the next scores.
-              if (s + 1 < x.n_i) {
-                const uint32_t ns = qs + 1 == kQoStages ? 0u : qs + 1;
-                const uint32_t nph = qs + 1 == kQoStages ? qph ^ 1u : qph;
-                if (!mbar_wait(&sm.q_full[ns], nph, guard)) { ok = false; break; }
-                tc_fence_after();
-                const uint64_t nst = sdesc_interleave(smem_addr(sm.rs[ns]), 0, 128);
-                mma_rows_by_rows<D>(tmem + 0, k_addr, smem_addr(sm.q[ns]), kIdS);
-                if constexpr (kRS) mma_ss(tmem + 0, sel_c, nst, kIdS, 1u);
-                mma_commit(&sm.s_ready);
-                if (!mbar_wait(&sm.o_full[ns], nph, guard)) { ok = false; break; }
-                tc_fence_after();
-                mma_rows_by_rows<D>(tmem + 128, v_addr, smem_addr(sm.d_o[ns]), kIdS);
-                if constexpr (kRS) mma_ss(tmem + 128, sel_d, nst, kIdS, 1u);
-                mma_commit(&sm.s_full);
-              }
-              // (dQ_i = dS K_j is issued by the second MMA thread, warp 3)
-            }
           }
           if constexpr (!kQ128 && !kQ64) {  // (kQ128: the reducer frees them; kQ64: above)
             mma_commit(&sm.q_empty[qs]);
@@ -661,17 +686,19 @@ __global__ void __launch_bounds__(640, 1)
     } else if (kQ64 && warp == 3 && lane == 0) {
       // --------------------------------- dQ issue (fused form, D = 64)
       // A second MMA-issuing thread: at d = 64 one thread cannot issue the
-      // 34 products of a step as fast as the tensor pipe runs them.  dQ_i =
-      // dS K_j reads only dS^T's shared tile (ds_ready, written after the
-      // grad warps published P^T and dS^T) and the K_j tile, and writes its
-      // own TMEM region (alternately [320,384) and [448,512), once the grad
-      // warps have drained dQ_{i-2} from it), so its order relative to the
-      // first thread's products does not matter; its completion is tracked
-      // by its own commits (dq_done, and kv_empty: K_j's slot is free only
-      // when both threads' products of the item are complete).
+      // 34 products of a step as fast as the tensor pipe runs them.  Per
+      // step it issues dK_i and then dQ_i = dS K_j, which reads
+      // only dS^T's shared tile (ds_ready, written after the grad warps
+      // published P^T and dS^T) and the K_j tile, and writes its own TMEM
+      // region (alternately [320,384) and [448,512), once the grad warps
+      // have drained dQ_{i-2} from it).  Its products' completion is
+      // tracked by its own commits (dk_done, q_empty, dq_done, and kv_empty:
+      // K_j's slot is free only when both threads' products of the item are
+      // complete).
       constexpr uint32_t kIdQ64 = idesc_bf16_f32(128, 64, 1, 1);  // dQ = dS K
+      constexpr uint32_t kIdG = idesc_bf16_f32(128, D, 0, 1);    // dK += dS^T Q_i
       const uint32_t k_addr = smem_addr(sm.k);
-      uint32_t kv_phase = 0;
+      uint32_t kv_phase = 0, qs = 0, qph = 0, p_phase = 0;
       int64_t n_dq = 0;
       bool issued = false;
       for (int64_t r = 0;; ++r) {
@@ -682,6 +709,27 @@ __global__ void __launch_bounds__(640, 1)
         kv_phase ^= 1;
         bool ok = true;
         for (int64_t s = 0; s < x.n_i; ++s) {
+          // dK_i += dS^T Q_i once the grad warps have published dS^T in TMEM
+          // (p_full), while the first thread issues dV_i and the next S^T;
+          // that thread waits for dk_done before the next dP^T overwrites
+          // the dS^T columns.  Q_i has then been read for the last time.
+          if (!mbar_wait(&sm.p_full, p_phase, guard)) { ok = false; break; }
+          p_phase ^= 1;
+          // (Q_i's load: already complete, as S^T_i has read it)
+          if (!mbar_wait(&sm.q_full[qs], qph, guard)) { ok = false; break; }
+          tc_fence_after();
+          {
+            const uint64_t bq0 = seq_b_base<D, false>(smem_addr(sm.q[qs]));
+            const uint32_t acc0 = s > 0 ? 1u : 0u;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ts(tmem + 384, tmem + 128 + packed_col(kk), bq0 + seq_b_step<D, false>(kk),
+                     kIdG, kk > 0 ? 1u : acc0);
+          }
+          mma_commit(&sm.dk_done);
+          mma_commit(&sm.q_empty[qs]);
+          issued = true;
+          if (++qs == kQoStages) { qs = 0; qph ^= 1; }
           const int buf = static_cast<int>(n_dq & 1);
           if (n_dq >= 2 &&
               !mbar_wait(&sm.dq_free[buf], static_cast<uint32_t>((n_dq - 2) >> 1) & 1u, guard)) {
@@ -728,9 +776,10 @@ __global__ void __launch_bounds__(640, 1)
         if (it >= p.n_items) break;
         const DkdvItem x = dkdv_item(p, it);
         bool ok = true;
+        DkdvCursor cur = dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s, ++m) {
           int64_t h, i;
-          dkdv_step(p, x, s, h, i);
+          dkdv_take(p, x, cur, h, i);
           if (!mbar_wait(&sm.stage_full, sf_phase, guard)) { ok = false; break; }
           sf_phase ^= 1;
           const uint8_t* src = reinterpret_cast<const uint8_t*>(sm.ds[kQ64 ? (m & 1) : 0]);
@@ -757,9 +806,10 @@ __global__ void __launch_bounds__(640, 1)
         if (it >= p.n_items) break;
         const DkdvItem x = dkdv_item(p, it);
         bool ok = true;
+        DkdvCursor cur = dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s) {
           int64_t h, i;
-          dkdv_step(p, x, s, h, i);
+          dkdv_take(p, x, cur, h, i);
           if (!mbar_wait(&sm.stage_full, sf_phase, guard)) { ok = false; break; }
           sf_phase ^= 1;
           // one bulk group per half: the Q_i slot (queries 0..63) is freed as
@@ -861,9 +911,10 @@ __global__ void __launch_bounds__(640, 1)
       const DkdvItem x = dkdv_item(p, it);
       const int64_t key_abs = p.kv_off + x.j * 128 + row;
       bool ok = true;
+      DkdvCursor cur = dkdv_first(x);
       for (int64_t s = 0; s < x.n_i; ++s) {
         int64_t h, i;
-        dkdv_step(p, x, s, h, i);
+        dkdv_take(p, x, cur, h, i);
         // P^T as soon as S^T is in (dP^T may still be in the tensor pipe)
         if (!mbar_wait(&sm.s_ready, s_phase, guard)) { ok = false; break; }
         if (!kRS && !mbar_wait(&sm.lse_full[ls], lph, guard)) { ok = false; break; }
