@@ -211,7 +211,7 @@ class ClockSampler:
         return False
 
     def summary(self):
-        sm, mx, reasons = [], None, set()
+        sm, mx, reasons, watts = [], None, set(), []
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -222,10 +222,15 @@ class ClockSampler:
                 mx = float(parts[2])
             except ValueError:
                 continue
+            try:
+                watts.append(float(parts[3]))
+            except ValueError:
+                pass
             for name, val in zip(names, parts[5:9]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "power_w": statistics.median(watts) if watts else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -370,11 +375,12 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
         barrier()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
         n_e2e = max(1, args.steps)
-        e2e_run(n_e2e)
-        b_.record(stream)
-        torch.cuda.synchronize()
+        with ClockSampler(local_rank) as e2e_clk:
+            a.record(stream)
+            e2e_run(n_e2e)
+            b_.record(stream)
+            torch.cuda.synchronize()
         if lsx.sync_status() != 0:
             raise RuntimeError("device status after the end-to-end steps")
         _, e2e_value = job_throughput(a.elapsed_time(b_), step_flops, n_e2e, world, dev)
@@ -382,7 +388,8 @@ def run_ours(args, rank, world, local_rank):
                "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "steps": n_e2e,
                "copies": "pinned host memory; two copy streams, overlapped with the "
-                         "neighbouring steps' compute"}
+                         "neighbouring steps' compute",
+               "clocks": e2e_clk.summary()}
 
     if rank != 0:
         return None
