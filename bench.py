@@ -496,6 +496,11 @@ def secondary(dev, pk):
       autograd_remat_32k
                   backward time through torch.autograd with the checkpoint
                   at the attention output vs at the layer input (re-run)
+      split_rows_32k_h1
+                  chunked forward of one head of 32K causal rows (64 query
+                  pairs for 152 SMs): rows split into key pieces
+                  merged by the LSE-weighted merge, against the unsplit
+                  launch (a workspace with room for the V copy only)
     """
     import torch
     import long_sequence_exact_gb300 as lsx
@@ -664,6 +669,35 @@ def secondary(dev, pk):
         "speedup": round(res["inputs"] / res["output"], 3),
         "workload": "causal_32k_ring through lsx.chunked_attention (torch.autograd)"}
     del x, q, k, v, d_o
+    torch.cuda.empty_cache()
+
+    import ctypes
+    from long_sequence_exact_gb300 import _lib
+    n1 = 32768
+    q1 = random_tensor((1, 1, n1, 128), 4242, 0.5, device=dev)
+    k1 = random_tensor((1, 1, n1, 128), 4243, 0.5, device=dev)
+    v1 = random_tensor((1, 1, n1, 128), 4244, 0.5, device=dev)
+    lib = _lib.load()
+    vq1, vk1 = _lib.view(q1), _lib.view(k1)
+    full = lib.attn_chunked_fwd_workspace_size(ctypes.byref(vq1), ctypes.byref(vk1), 4096, 1)
+    base = lib.attn_chunk_fwd_workspace_size(ctypes.byref(vq1), ctypes.byref(vk1))
+    ws_full = torch.empty(int(full), dtype=torch.uint8, device=dev)
+    ws_base = torch.empty(int(base), dtype=torch.uint8, device=dev)
+    o1 = torch.empty_like(q1)
+    l1 = torch.empty((1, 1, n1), dtype=torch.float32, device=dev)
+    t_split = timed(lambda: lsx.chunked_fwd(q1, k1, v1, 4096, True, out=o1, lse=l1,
+                                            workspace=ws_full))
+    t_whole = timed(lambda: lsx.chunked_fwd(q1, k1, v1, 4096, True, out=o1, lse=l1,
+                                            workspace=ws_base))
+    f1, _ = flops(1, 1, n1, 128, True)
+    out["split_rows_32k_h1"] = {
+        "split": full > base,
+        "ms_split": round(t_split, 3), "ms_unsplit": round(t_whole, 3),
+        "speedup": round(t_whole / t_split, 3),
+        "tflops_split": round(f1 / (t_split / 1e3) / 1e12, 1),
+        "frac_split": round(f1 / (t_split / 1e3) / 1e12 / pk["bf16_sustained"], 4),
+        "workload": "B=1 H=1 N=32768 d=128 causal, forward (chunked_fwd)"}
+    del q1, k1, v1, o1, l1, ws_full, ws_base
     torch.cuda.empty_cache()
     return out
 

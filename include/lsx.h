@@ -256,10 +256,21 @@ int attn_chunk_bwd_noalloc(const lsx_tensor* q, const lsx_tensor* k,
  * stopping, carrying one online softmax across the chunk edges, which equals
  * computing each chunk pair's partial and combining the partials with
  * attn_merge in that order (the merge is associative: Lean Attention
- * abstract).  No partials are written and no row is split; the forward
- * workspace holds only the key-contiguous copy of V (as attn_chunk_fwd), the
- * backward workspace what attn_chunk_bwd uses.  Same dtypes as the chunk
- * calls.
+ * abstract).  Same dtypes as the chunk calls.
+ *
+ * Forward, split rows: when the query pairs (256 rows each) number fewer than
+ * the SMs (few heads, long rows) and the rows are bf16 with D = 64 or 128,
+ * every pair's visible key tiles are cut into pieces (about four pieces of
+ * work per SM, at most 32 pieces per row).  Each piece writes its
+ * normalised partial (fp32 O, LSE) to the workspace, and one more kernel
+ * combines each row's pieces by the LSE-weighted merge (the stream-K style
+ * split of the Lean Attention abstract; the result equals the unsplit one up
+ * to fp32 rounding of the merge).  attn_chunked_fwd_workspace_size counts
+ * those partials (for the current device's SM count); a workspace only as
+ * large as attn_chunk_fwd_workspace_size, or none, runs the unsplit launch.
+ * Otherwise the forward workspace holds the key-contiguous copy of V (as
+ * attn_chunk_fwd) and the backward workspace what attn_chunk_bwd uses; the
+ * backward never splits.
  * ---------------------------------------------------------------------- */
 size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal);

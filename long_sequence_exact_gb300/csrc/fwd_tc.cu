@@ -95,15 +95,34 @@ struct FwdParams {
   const uint8_t* bmask;  // [n_qtiles][n_kb]
   int64_t n_qtiles, n_kb;
   uint64_t* trace;  // per-CTA schedule record (NULL: not traced)
+  // rows split into key pieces (piece_w 0: not split); n_items counts
+  // kmax * n_qpairs * B * Hq items then, piece-major
+  int64_t piece_w, kmax;
+  float* part_o;    // [kmax][B][Hq][Lq][D] fp32
+  float* part_lse;  // [kmax][B][Hq][Lq]
 };
 
 struct Item {
   int64_t b, h, hk, pair;
-  int64_t nkv[2];
+  int64_t nkv[2];  // key tiles this item visits for query tile 2 pair + t
+  int64_t j0;      // position of its first key tile (0 unless split)
+  int64_t piece;   // piece of the rows (0 unless split)
+  bool empty;      // a piece past the pair's last visible key tile: skipped
 };
 
 __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
   Item x;
+  x.j0 = 0;
+  x.piece = 0;
+  x.empty = false;
+  if (p.piece_w > 0) {
+    // piece-major: every pair's first piece (pairs longest first), then
+    // every pair's second, ...: full pieces come before a round's short and
+    // empty ones, which the snake deal then spreads over the CTAs
+    const int64_t per_piece = p.n_qpairs * p.B * p.Hq;
+    x.piece = it / per_piece;
+    it -= x.piece * per_piece;
+  }
   int64_t rank, bh;
   banded_item(it, p.n_qpairs, p.B * p.Hq, &rank, &bh);
   x.pair = p.n_qpairs - 1 - rank;
@@ -114,13 +133,21 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
     x.nkv[t] = p.pair_list == nullptr
                    ? fwd_kv_tiles(2 * x.pair + t, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal)
                    : (2 * x.pair + t < p.n_qtiles ? p.pair_count[x.pair] : 0);
+  if (p.piece_w > 0) {
+    x.j0 = x.piece * p.piece_w;
+    x.empty = x.j0 >= (x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1]);
+    for (int t = 0; t < 2; ++t) {
+      const int64_t n = x.nkv[t] - x.j0;
+      x.nkv[t] = n < 0 ? 0 : (n > p.piece_w ? p.piece_w : n);
+    }
+  }
   return x;
 }
 
 // Key tile visited at position j of an item (the j-th listed tile when the
 // attention is block-sparse).
 __device__ __forceinline__ int64_t key_tile(const FwdParams& p, const Item& x, int64_t j) {
-  return p.pair_list == nullptr ? j : p.pair_list[x.pair * p.n_kb + j];
+  return p.pair_list == nullptr ? x.j0 + j : p.pair_list[x.pair * p.n_kb + j];
 }
 
 // Wait that ignores the abort flag but keeps the time bound (used at exit).
@@ -194,6 +221,7 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
       const Item x = decode_item(p, it);
+      if (x.empty) continue;  // (every role skips the same items)
       const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
       if (!mbar_wait(&sm.q_empty, qe_phase ^ 1, guard)) break;
       qe_phase ^= 1;
@@ -260,6 +288,7 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
       const Item x = decode_item(p, it);
+      if (x.empty) continue;
       const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
       if (!mbar_wait(&sm.q_full, q_phase, guard)) break;
       q_phase ^= 1;
@@ -349,11 +378,13 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t it = snake_item(blockIdx.x, r, gridDim.x);
       if (it >= p.n_items) break;
       int nkv;
-      int64_t pair;
+      int64_t pair, j0;
       {
         const Item x = decode_item(p, it);
+        if (x.empty) continue;
         nkv = static_cast<int>(x.nkv[t]);
         pair = x.pair;
+        j0 = x.j0;
       }
       const int64_t qr0 = (2 * pair + t) * 128;
       float m = kNegInf, l = 0.f;
@@ -382,8 +413,9 @@ __global__ void __launch_bounds__(384, 1)
             s[96 + i] = __uint_as_float(u3[i]);
           }
         }
+        // (the key_tile position: j0 + j, or the j-th listed tile)
         const int64_t kb =
-            (p.pair_list == nullptr ? j : p.pair_list[pair * p.n_kb + j]) * int64_t{128};
+            (p.pair_list == nullptr ? j0 + j : p.pair_list[pair * p.n_kb + j]) * int64_t{128};
         // a listed tile whose block this query tile does not have: all masked
         const bool blk_off =
             p.bmask != nullptr && p.bmask[(2 * pair + t) * p.n_kb + kb / 128] == 0;
@@ -464,6 +496,9 @@ __global__ void __launch_bounds__(384, 1)
       const Item x = decode_item(p, it);
       const int64_t qrow = qr0 + row;
       const bool valid = qrow < p.Lq;
+      // split rows: this piece's normalised partial goes to its fp32 slot
+      const bool split = p.piece_w > 0;
+      const int64_t prow = ((x.piece * p.B + x.b) * p.Hq + x.h) * p.Lq + qrow;
       if (nkv > 0) {
         if (!wait(&sm.o_full[t], (pv_count - 1) & 1)) break;
         tc_fence_after();
@@ -497,9 +532,10 @@ __global__ void __launch_bounds__(384, 1)
         float ov[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(u[i]) * inv * w_new;
-        const int64_t base = x.b * p.o_sb + x.h * p.o_sh + qrow * p.o_sn + cc * 32;
-        if (p.o_f32) {
-          float* dst = static_cast<float*>(p.o) + base;
+        const int64_t base =
+            split ? prow * D + cc * 32 : x.b * p.o_sb + x.h * p.o_sh + qrow * p.o_sn + cc * 32;
+        if (split || p.o_f32) {
+          float* dst = (split ? p.part_o : static_cast<float*>(p.o)) + base;
           if (p.accumulate) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -538,7 +574,12 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       }
-      if (valid) p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn] = lse_new;
+      if (valid) {
+        if (split)
+          p.part_lse[prow] = lse_new;
+        else
+          p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn] = lse_new;
+      }
     }
   }
 
@@ -557,7 +598,8 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
                     const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                     int causal, float scale, const lsx_tensor& o,
                     const lsx_tensor& lse, int accumulate, void* vt,
-                    const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl) {
+                    const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl,
+                    const FwdSplit* split) {
   CUtensorMap tq, tk, tv;
   if (!make_map_bf16_4d(&tq, q.data, q.B, q.H, q.N, q.D, q.stride_b, q.stride_h,
                         q.stride_n, 128) ||
@@ -592,6 +634,19 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
   p.pair_list = bl ? bl->pair_list : nullptr;
   p.bmask = bl ? bl->mask : nullptr;
   p.n_kb = bl ? bl->n_kb : 0;
+  p.piece_w = 0;
+  p.kmax = 1;
+  p.part_o = nullptr;
+  p.part_lse = nullptr;
+  if (split != nullptr && split->piece_w > 0) {
+    // (never with block lists or accumulation: the chunked call alone splits)
+    if (bl != nullptr || accumulate || split->kmax < 1) return LSX_ERR_UNSUPPORTED;
+    p.piece_w = split->piece_w;
+    p.kmax = split->kmax;
+    p.part_o = split->part_o;
+    p.part_lse = split->part_lse;
+    p.n_items *= p.kmax;
+  }
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
   auto kern = vt != nullptr ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -613,13 +668,14 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
                   const lsx_tensor& lse, int accumulate, void* vt,
-                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl) {
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl,
+                  const FwdSplit* split) {
   if (q.D == 128)
     return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                                accumulate, vt, ctx, s, bl);
+                                accumulate, vt, ctx, s, bl, split);
   if (q.D == 64)
     return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                               accumulate, vt, ctx, s, bl);
+                               accumulate, vt, ctx, s, bl, split);
   return LSX_ERR_UNSUPPORTED;
 }
 

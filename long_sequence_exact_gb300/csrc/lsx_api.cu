@@ -400,10 +400,64 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
 }
 
 // ------------------------------------------- whole-sequence chunked calls
+// Rows split into key pieces (Lean Attention abstract: the partials of one
+// row, computed by different workers, combine exactly by the associative
+// merge).  The persistent forward deals its query pairs over the SMs
+// longest first; with fewer pairs than SMs (few heads, long rows) some SMs
+// have nothing to do and the longest rows set the launch's time.  The pairs'
+// visible key tiles are then cut into pieces of piece_w tiles, sized for
+// about four pieces of work per SM and at most 32 pieces per row (one warp
+// merges them), and the merge kernel combines each row's pieces.  (Measured:
+// one 32K head, 128 pairs, 0.50 -> 0.36 ms; with 256 pairs the unsplit deal
+// was already balanced and splitting lost.)
+static bool plan_split(const lsx_tensor& q, const lsx_tensor& k, int causal, int sm_count,
+                       FwdSplit* out) {
+  if (q.dtype != LSX_BF16 || q.N <= 0 || k.N <= 0 || sm_count <= 0) return false;
+  if (q.D != 64 && q.D != 128) return false;
+  const int64_t n_pairs = ceil_div(q.N, 256);
+  if (q.B * q.H * n_pairs >= static_cast<int64_t>(sm_count)) return false;
+  int64_t total = 0, longest = 0;
+  for (int64_t pr = 0; pr < n_pairs; ++pr) {
+    const int64_t a = fwd_kv_tiles(2 * pr, q.N, k.N, 0, 0, causal);
+    const int64_t b = fwd_kv_tiles(2 * pr + 1, q.N, k.N, 0, 0, causal);
+    const int64_t m = a > b ? a : b;
+    total += m;
+    if (m > longest) longest = m;
+  }
+  total *= q.B * q.H;
+  int64_t w = ceil_div(total, 4 * static_cast<int64_t>(sm_count));
+  if (w < 4) w = 4;
+  if (ceil_div(longest, w) > 32) w = ceil_div(longest, 32);
+  const int64_t kmax = ceil_div(longest, w);
+  if (kmax < 2) return false;
+  out->piece_w = w;
+  out->kmax = kmax;
+  return true;
+}
+
+// bytes of the partials of a split (O, then LSE), each region 256-aligned
+static size_t split_bytes(const lsx_tensor& q, const FwdSplit& sp, size_t* o_bytes) {
+  const size_t rows = static_cast<size_t>(sp.kmax) * q.B * q.H * q.N;
+  *o_bytes = (rows * q.D * sizeof(float) + 255) / 256 * 256;
+  return *o_bytes + (rows * sizeof(float) + 255) / 256 * 256;
+}
+
+static int current_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal) {
-  (void)chunk_len; (void)causal;
-  return attn_chunk_fwd_workspace_size(q, k);
+  (void)chunk_len;
+  const size_t base = attn_chunk_fwd_workspace_size(q, k);
+  if (base == 0) return 0;
+  FwdSplit sp;
+  if (!plan_split(*q, *k, causal, current_sm_count(), &sp)) return base;
+  size_t o_bytes;
+  return base + split_bytes(*q, sp, &o_bytes);
 }
 
 int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
@@ -414,8 +468,31 @@ int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
   LSX_TRY(check_qkv(q, k, v));
   if (q->N != k->N) return LSX_ERR_SHAPE;
   if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
-  // One persistent launch covers every visible chunk pair (see fwd_tc.cu);
-  // the chunk length sets no boundary the online softmax could not cross.
+  // Split the rows when the workspace holds their partials (see plan_split);
+  // otherwise one persistent launch covers every visible chunk pair (see
+  // fwd_tc.cu): the chunk length sets no boundary the online softmax could
+  // not cross.
+  FwdSplit sp;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const size_t base = attn_chunk_fwd_workspace_size(q, k);
+  size_t o_bytes = 0;
+  if (workspace != nullptr && base > 0 && plan_split(*q, *k, causal, ctx.sm_count, &sp) &&
+      workspace_bytes >= base + split_bytes(*q, sp, &o_bytes)) {
+    LSX_TRY(check_view(o));
+    if (o->B != q->B || o->H != q->H || o->N != q->N || o->D != q->D) return LSX_ERR_SHAPE;
+    LSX_TRY(check_row_aligned(o));
+    LSX_TRY(check_lse(lse, q));
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return LSX_ERR_ALIGN;
+    char* ws = static_cast<char*>(workspace);
+    sp.part_o = reinterpret_cast<float*>(ws + base);
+    sp.part_lse = reinterpret_cast<float*>(ws + base + o_bytes);
+    const float sc = resolve_scale(scale, q->D);
+    cudaStream_t s = as_stream(stream);
+    LSX_TRY(launch_fwd_tc(*q, *k, *v, 0, 0, causal != 0, sc, *o, *lse, 0, workspace, ctx, s,
+                          nullptr, &sp));
+    return launch_merge_pieces(sp, 0, 0, causal != 0, k->N, *o, *lse, ctx, s);
+  }
   return attn_chunk_fwd(q, k, v, 0, 0, causal, scale, o, lse, 0, workspace,
                         workspace_bytes, stream);
 }

@@ -246,6 +246,60 @@ __global__ void __launch_bounds__(256) tree_merge_warp_kernel(
   }
 }
 
+// The pieces of split rows (FwdSplit): one warp per row, lane p holding
+// piece p's LSE.  A row has as many pieces as its query pair: ceil(its
+// pair's visible key tiles / piece_w), from the same causal geometry the
+// forward used; slot p of the partials sits p * B * H * Lq rows on.  Pieces
+// are combined in the order p = 0, 1, ..., like tree_merge_warp_kernel.
+template <int E>
+__global__ void __launch_bounds__(256) merge_pieces_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_lse, int64_t piece_w,
+    int64_t Lk, int64_t q_off, int64_t kv_off, int causal, lsx_tensor oo, lsx_tensor lo,
+    int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const RowIdx ri{oo.H, oo.N};
+  for (int64_t row = w0; row < rows; row += nw) {
+    int64_t b, h, n;
+    ri.split(row, b, h, n);
+    const int64_t pair = (n / 128) / 2;
+    const int64_t t0 = fwd_kv_tiles(2 * pair, oo.N, Lk, q_off, kv_off, causal);
+    const int64_t t1 = fwd_kv_tiles(2 * pair + 1, oo.N, Lk, q_off, kv_off, causal);
+    const int64_t tiles = t0 > t1 ? t0 : t1;
+    const int n_parts = static_cast<int>((tiles + piece_w - 1) / piece_w);
+    const float x = lane < n_parts ? part_lse[lane * rows + row] : kNegInf;
+    float m = x;
+    for (int s = 16; s > 0; s >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+    const float wl = (m == kNegInf || lane >= n_parts) ? 0.f : expf(x - m);
+    float tot = wl;
+    for (int s = 16; s > 0; s >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, s);
+    Vec<E> acc;
+    for (int e = 0; e < E; ++e) acc.v[e] = 0.f;
+    if (m != kNegInf) {
+      for (int p0 = 0; p0 < n_parts; p0 += 4) {
+        Vec<E> xs[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (p0 + u < n_parts)
+            xs[u] = load_row<E>(part_o, LSX_F32, ((p0 + u) * rows + row) * (32 * E), lane);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float w = __shfl_sync(0xffffffffu, wl, (p0 + u) & 31);
+          if (p0 + u < n_parts)
+            for (int e = 0; e < E; ++e) acc.v[e] = fmaf(w, xs[u].v[e], acc.v[e]);
+        }
+      }
+      const float inv = 1.f / tot;
+      for (int e = 0; e < E; ++e) acc.v[e] *= inv;
+    }
+    store_row<E>(oo.data, oo.dtype, view_off(oo, b, h, n), lane, acc);
+    if (lane == 0)
+      static_cast<float*>(lo.data)[view_off(lo, b, h, n)] =
+          (m == kNegInf) ? kNegInf : m + logf(tot);
+  }
+}
+
 // One block of 8 warps per row for many partials: warp w takes partials
 // p = w, w + 8, ...; the 8 warp sums are combined in warp order.
 template <int E>
@@ -482,6 +536,21 @@ int launch_tree_merge(const lsx_tensor& op, int64_t pso, const lsx_tensor& lp,
                              grid_for_rows(tree_merge_block_kernel<E>, rows, ctx, 1), 256, 0, s>>>(
                              op, pso, lp, psl, n_parts, oo, lo, rows));
   }
+  timing_end(kKidTreeMerge, s);
+  return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
+}
+
+int launch_merge_pieces(const FwdSplit& split, int64_t q_off, int64_t kv_off, int causal,
+                        int64_t Lk, const lsx_tensor& o, const lsx_tensor& lse,
+                        const DeviceCtx& ctx, cudaStream_t s) {
+  const int64_t rows = o.B * o.H * o.N;
+  if (rows == 0) return LSX_OK;
+  if (split.piece_w <= 0 || split.kmax < 1 || split.kmax > 32) return LSX_ERR_UNSUPPORTED;
+  timing_begin(kKidTreeMerge, s);
+  LSX_DISPATCH_E(o.D, merge_pieces_kernel<E><<<grid_for_rows(merge_pieces_kernel<E>, rows, ctx, 8),
+                                                256, 0, s>>>(split.part_o, split.part_lse,
+                                                             split.piece_w, Lk, q_off, kv_off,
+                                                             causal, o, lse, rows));
   timing_end(kKidTreeMerge, s);
   return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
 }
