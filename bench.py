@@ -45,7 +45,8 @@ PKG = os.path.join(ROOT, "long_sequence_exact_gb300")
 # beside it (profiles/*.md, "traffic:" lines), so a changed kernel reports no
 # stale traffic.
 KERNEL_SOURCES = {
-    "fwd_tc": ("csrc/fwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+    "fwd_tc": ("csrc/fwd_tc.cu", "csrc/fwd_split.h", "csrc/ptx.cuh", "csrc/internal.h",
+               "csrc/tma_host.h"),
     "bwd_fused_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
     "bwd_dkdv_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
     "bwd_dq_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),

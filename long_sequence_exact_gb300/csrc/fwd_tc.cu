@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "fwd_split.h"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -105,23 +106,28 @@ struct FwdParams {
 struct Item {
   int64_t b, h, hk, pair;
   int64_t nkv[2];  // key tiles this item visits for query tile 2 pair + t
-  int64_t j0;      // position of its first key tile (0 unless split)
-  int64_t piece;   // piece of the rows (0 unless split)
-  bool empty;      // a piece past the pair's last visible key tile: skipped
 };
 
-__device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
+// The piece of split rows an item is (kept apart from Item: its fields
+// alone cost the unsplit kernel registers, even unused).
+struct Piece {
+  int64_t j0 = 0;     // position of its first key tile
+  int64_t piece = 0;  // slot of its partials
+  bool empty = false; // past the pair's last visible key tile: skipped
+};
+
+// (kSplit: rows split into key pieces; a template parameter, so that the
+// unsplit kernel carries none of it)
+template <bool kSplit>
+__device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it, Piece* pc = nullptr) {
   Item x;
-  x.j0 = 0;
-  x.piece = 0;
-  x.empty = false;
-  if (p.piece_w > 0) {
+  if constexpr (kSplit) {
     // piece-major: every pair's first piece (pairs longest first), then
     // every pair's second, ...: full pieces come before a round's short and
     // empty ones, which the snake deal then spreads over the CTAs
     const int64_t per_piece = p.n_qpairs * p.B * p.Hq;
-    x.piece = it / per_piece;
-    it -= x.piece * per_piece;
+    pc->piece = it / per_piece;
+    it -= pc->piece * per_piece;
   }
   int64_t rank, bh;
   banded_item(it, p.n_qpairs, p.B * p.Hq, &rank, &bh);
@@ -133,11 +139,11 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
     x.nkv[t] = p.pair_list == nullptr
                    ? fwd_kv_tiles(2 * x.pair + t, p.Lq, p.Lk, p.q_off, p.kv_off, p.causal)
                    : (2 * x.pair + t < p.n_qtiles ? p.pair_count[x.pair] : 0);
-  if (p.piece_w > 0) {
-    x.j0 = x.piece * p.piece_w;
-    x.empty = x.j0 >= (x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1]);
+  if constexpr (kSplit) {
+    pc->j0 = pc->piece * p.piece_w;
+    pc->empty = pc->j0 >= (x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1]);
     for (int t = 0; t < 2; ++t) {
-      const int64_t n = x.nkv[t] - x.j0;
+      const int64_t n = x.nkv[t] - pc->j0;
       x.nkv[t] = n < 0 ? 0 : (n > p.piece_w ? p.piece_w : n);
     }
   }
@@ -146,8 +152,9 @@ __device__ __forceinline__ Item decode_item(const FwdParams& p, int64_t it) {
 
 // Key tile visited at position j of an item (the j-th listed tile when the
 // attention is block-sparse).
-__device__ __forceinline__ int64_t key_tile(const FwdParams& p, const Item& x, int64_t j) {
-  return p.pair_list == nullptr ? x.j0 + j : p.pair_list[x.pair * p.n_kb + j];
+__device__ __forceinline__ int64_t key_tile(const FwdParams& p, const Item& x, int64_t j,
+                                            int64_t j0) {
+  return p.pair_list == nullptr ? j0 + j : p.pair_list[x.pair * p.n_kb + j];
 }
 
 // Wait that ignores the abort flag but keeps the time bound (used at exit).
@@ -159,7 +166,7 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
-template <int D, bool kVt>
+template <int D, bool kVt, bool kSplit>
 __global__ void __launch_bounds__(384, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_k,
@@ -220,8 +227,9 @@ __global__ void __launch_bounds__(384, 1)
     for (;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
-      const Item x = decode_item(p, it);
-      if (x.empty) continue;  // (every role skips the same items)
+      Piece pc;
+      const Item x = decode_item<kSplit>(p, it, &pc);
+      if (kSplit && pc.empty) continue;  // (every role skips the same items)
       const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
       if (!mbar_wait(&sm.q_empty, qe_phase ^ 1, guard)) break;
       qe_phase ^= 1;
@@ -233,7 +241,7 @@ __global__ void __launch_bounds__(384, 1)
                       static_cast<int>(x.h), static_cast<int>(x.b));
       bool ok = true;
       for (int64_t j = 0; j < nkv; ++j) {
-        const int64_t kt = key_tile(p, x, j);
+        const int64_t kt = key_tile(p, x, j, kSplit ? pc.j0 : 0);
         if (!mbar_wait(&sm.k_empty[stage], phase ^ 1, guard)) { ok = false; break; }
         mbar_arrive_expect_tx(&sm.k_full[stage], Cfg::kTileBytes);
         for (int sub = 0; sub < Cfg::kSub; ++sub)
@@ -287,8 +295,9 @@ __global__ void __launch_bounds__(384, 1)
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
-      const Item x = decode_item(p, it);
-      if (x.empty) continue;
+      Piece pc;
+      const Item x = decode_item<kSplit>(p, it, &pc);
+      if (kSplit && pc.empty) continue;
       const int64_t nkv = x.nkv[0] > x.nkv[1] ? x.nkv[0] : x.nkv[1];
       if (!mbar_wait(&sm.q_full, q_phase, guard)) break;
       q_phase ^= 1;
@@ -378,13 +387,14 @@ __global__ void __launch_bounds__(384, 1)
       const int64_t it = snake_item(blockIdx.x, r, gridDim.x);
       if (it >= p.n_items) break;
       int nkv;
-      int64_t pair, j0;
+      int64_t pair, j0 = 0;
       {
-        const Item x = decode_item(p, it);
-        if (x.empty) continue;
+        Piece pc;
+        const Item x = decode_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;
         nkv = static_cast<int>(x.nkv[t]);
         pair = x.pair;
-        j0 = x.j0;
+        if constexpr (kSplit) j0 = pc.j0;
       }
       const int64_t qr0 = (2 * pair + t) * 128;
       float m = kNegInf, l = 0.f;
@@ -415,7 +425,8 @@ __global__ void __launch_bounds__(384, 1)
         }
         // (the key_tile position: j0 + j, or the j-th listed tile)
         const int64_t kb =
-            (p.pair_list == nullptr ? j0 + j : p.pair_list[pair * p.n_kb + j]) * int64_t{128};
+            (p.pair_list == nullptr ? (kSplit ? j0 + j : j) : p.pair_list[pair * p.n_kb + j]) *
+            int64_t{128};
         // a listed tile whose block this query tile does not have: all masked
         const bool blk_off =
             p.bmask != nullptr && p.bmask[(2 * pair + t) * p.n_kb + kb / 128] == 0;
@@ -493,12 +504,13 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) break;
       // --------------------------------------------------------- epilogue
-      const Item x = decode_item(p, it);
+      Piece pc;
+      const Item x = decode_item<kSplit>(p, it, &pc);
       const int64_t qrow = qr0 + row;
       const bool valid = qrow < p.Lq;
       // split rows: this piece's normalised partial goes to its fp32 slot
-      const bool split = p.piece_w > 0;
-      const int64_t prow = ((x.piece * p.B + x.b) * p.Hq + x.h) * p.Lq + qrow;
+      int64_t prow = 0;
+      if constexpr (kSplit) prow = ((pc.piece * p.B + x.b) * p.Hq + x.h) * p.Lq + qrow;
       if (nkv > 0) {
         if (!wait(&sm.o_full[t], (pv_count - 1) & 1)) break;
         tc_fence_after();
@@ -532,10 +544,13 @@ __global__ void __launch_bounds__(384, 1)
         float ov[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) ov[i] = __uint_as_float(u[i]) * inv * w_new;
-        const int64_t base =
-            split ? prow * D + cc * 32 : x.b * p.o_sb + x.h * p.o_sh + qrow * p.o_sn + cc * 32;
-        if (split || p.o_f32) {
-          float* dst = (split ? p.part_o : static_cast<float*>(p.o)) + base;
+        int64_t base;
+        if constexpr (kSplit)
+          base = prow * D + cc * 32;
+        else
+          base = x.b * p.o_sb + x.h * p.o_sh + qrow * p.o_sn + cc * 32;
+        if (kSplit || p.o_f32) {
+          float* dst = (kSplit ? p.part_o : static_cast<float*>(p.o)) + base;
           if (p.accumulate) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
@@ -575,7 +590,7 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
       if (valid) {
-        if (split)
+        if constexpr (kSplit)
           p.part_lse[prow] = lse_new;
         else
           p.lse[x.b * p.l_sb + x.h * p.l_sh + qrow * p.l_sn] = lse_new;
@@ -648,7 +663,10 @@ int launch_fwd_tc_d(const lsx_tensor& q, const lsx_tensor& k,
     p.n_items *= p.kmax;
   }
   const size_t smem = sizeof(FwdSmem<D>) + 1024;
-  auto kern = vt != nullptr ? fwd_tc_kernel<D, true> : fwd_tc_kernel<D, false>;
+  auto kern = p.piece_w > 0 ? (vt != nullptr ? fwd_tc_kernel<D, true, true>
+                                             : fwd_tc_kernel<D, false, true>)
+                           : (vt != nullptr ? fwd_tc_kernel<D, true, false>
+                                            : fwd_tc_kernel<D, false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return LSX_ERR_LAUNCH;
@@ -668,14 +686,27 @@ int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
                   const lsx_tensor& lse, int accumulate, void* vt,
-                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl,
-                  const FwdSplit* split) {
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl) {
   if (q.D == 128)
     return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                                accumulate, vt, ctx, s, bl, split);
+                                accumulate, vt, ctx, s, bl, nullptr);
   if (q.D == 64)
     return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse,
-                               accumulate, vt, ctx, s, bl, split);
+                               accumulate, vt, ctx, s, bl, nullptr);
+  return LSX_ERR_UNSUPPORTED;
+}
+
+int launch_fwd_tc_split(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
+                        int64_t q_off, int64_t kv_off, int causal, float scale,
+                        const lsx_tensor& o, const lsx_tensor& lse, void* vt,
+                        const FwdSplit& split, const DeviceCtx& ctx, cudaStream_t s) {
+  if (split.piece_w <= 0) return LSX_ERR_UNSUPPORTED;
+  if (q.D == 128)
+    return launch_fwd_tc_d<128>(q, k, v, q_off, kv_off, causal, scale, o, lse, 0, vt, ctx, s,
+                                nullptr, &split);
+  if (q.D == 64)
+    return launch_fwd_tc_d<64>(q, k, v, q_off, kv_off, causal, scale, o, lse, 0, vt, ctx, s,
+                               nullptr, &split);
   return LSX_ERR_UNSUPPORTED;
 }
 

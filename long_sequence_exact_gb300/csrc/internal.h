@@ -150,29 +150,11 @@ int build_block_lists(const uint8_t* mask, int64_t lq, int64_t lk, int causal, v
 // key-contiguous copy of V first, which the P.V product reads faster.
 size_t fwd_tc_workspace_bytes(const lsx_tensor& v);
 // With bl non-NULL, each item visits only the key tiles of its block lists.
-// Rows split into key pieces (the forward of few long rows): each query
-// pair's visible key tiles are cut into pieces of piece_w tiles; piece i of
-// every pair writes its normalised partial (fp32 O, LSE) to slot i of
-// part_o [kmax][B][Hq][Lq][D] and part_lse [kmax][B][Hq][Lq], which
-// launch_merge_pieces then combines row by row.
-struct FwdSplit {
-  int64_t piece_w = 0;  // key tiles per piece
-  int64_t kmax = 0;     // pieces of the longest pair
-  float* part_o = nullptr;
-  float* part_lse = nullptr;
-};
-
 int launch_fwd_tc(const lsx_tensor& q, const lsx_tensor& k,
                   const lsx_tensor& v, int64_t q_off, int64_t kv_off,
                   int causal, float scale, const lsx_tensor& o,
                   const lsx_tensor& lse, int accumulate, void* vt,
-                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr,
-                  const FwdSplit* split = nullptr);
-// The LSE-weighted merge of each row's pieces (as many as its query pair has:
-// ceil(visible key tiles / piece_w)) into o (bf16 or f32) and lse.
-int launch_merge_pieces(const FwdSplit& split, int64_t q_off, int64_t kv_off, int causal,
-                        int64_t Lk, const lsx_tensor& o, const lsx_tensor& lse,
-                        const DeviceCtx& ctx, cudaStream_t s);
+                  const DeviceCtx& ctx, cudaStream_t s, const BlockLists* bl = nullptr);
 
 // tcgen05 tensor-core backward (bf16 inputs).  Unless the deterministic
 // mode is set, one kernel computes dK, dV and dQ (D = 128 or 64), adding each

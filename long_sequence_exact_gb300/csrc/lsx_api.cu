@@ -11,6 +11,7 @@
 #include <mutex>
 #include <vector>
 
+#include "fwd_split.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -489,8 +490,8 @@ int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
     sp.part_lse = reinterpret_cast<float*>(ws + base + o_bytes);
     const float sc = resolve_scale(scale, q->D);
     cudaStream_t s = as_stream(stream);
-    LSX_TRY(launch_fwd_tc(*q, *k, *v, 0, 0, causal != 0, sc, *o, *lse, 0, workspace, ctx, s,
-                          nullptr, &sp));
+    LSX_TRY(launch_fwd_tc_split(*q, *k, *v, 0, 0, causal != 0, sc, *o, *lse, workspace, sp,
+                                ctx, s));
     return launch_merge_pieces(sp, 0, 0, causal != 0, k->N, *o, *lse, ctx, s);
   }
   return attn_chunk_fwd(q, k, v, 0, 0, causal, scale, o, lse, 0, workspace,

@@ -14,6 +14,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "fwd_split.h"
 #include "internal.h"
 
 namespace lsx {
