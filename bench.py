@@ -47,9 +47,12 @@ PKG = os.path.join(ROOT, "long_sequence_exact_gb300")
 KERNEL_SOURCES = {
     "fwd_tc": ("csrc/fwd_tc.cu", "csrc/fwd_split.h", "csrc/ptx.cuh", "csrc/internal.h",
                "csrc/tma_host.h"),
-    "bwd_fused_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
-    "bwd_dkdv_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
-    "bwd_dq_tc": ("csrc/bwd_tc.cu", "csrc/ptx.cuh", "csrc/internal.h", "csrc/tma_host.h"),
+    "bwd_fused_tc": ("csrc/bwd_tc.cu", "csrc/bwd_split.h", "csrc/ptx.cuh", "csrc/internal.h",
+                     "csrc/tma_host.h"),
+    "bwd_dkdv_tc": ("csrc/bwd_tc.cu", "csrc/bwd_split.h", "csrc/ptx.cuh", "csrc/internal.h",
+                    "csrc/tma_host.h"),
+    "bwd_dq_tc": ("csrc/bwd_tc.cu", "csrc/bwd_split.h", "csrc/ptx.cuh", "csrc/internal.h",
+                  "csrc/tma_host.h"),
 }
 TRACE_KERNELS = {0: "fwd_tc", 1: "bwd_dkdv_tc", 2: "bwd_dq_tc", 12: "bwd_fused_tc"}
 
@@ -501,7 +504,10 @@ def secondary(dev, pk):
                   chunked forward of one head of 32K causal rows (64 query
                   pairs for 152 SMs): rows split into key pieces
                   merged by the LSE-weighted merge, against the unsplit
-                  launch (a workspace with room for the V copy only)
+                  launch (a workspace with room for the V copy only); and
+                  the chunked backward of one head of 16K causal rows (128
+                  key-tile items): key columns split, partial dK / dV
+                  summed, against the unsplit launch
     """
     import torch
     import long_sequence_exact_gb300 as lsx
@@ -699,6 +705,30 @@ def secondary(dev, pk):
         "frac_split": round(f1 / (t_split / 1e3) / 1e12 / pk["bf16_sustained"], 4),
         "workload": "B=1 H=1 N=32768 d=128 causal, forward (chunked_fwd)"}
     del q1, k1, v1, o1, l1, ws_full, ws_base
+    n2 = 16384
+    q2 = random_tensor((1, 1, n2, 128), 4252, 0.5, device=dev)
+    k2 = random_tensor((1, 1, n2, 128), 4253, 0.5, device=dev)
+    v2 = random_tensor((1, 1, n2, 128), 4254, 0.5, device=dev)
+    do2 = random_tensor((1, 1, n2, 128), 4255, 1.0, device=dev)
+    o2, l2 = lsx.chunked_fwd(q2, k2, v2, 4096, True)
+    vq2, vk2 = _lib.view(q2), _lib.view(k2)
+    full2 = lib.attn_chunked_bwd_workspace_size(ctypes.byref(vq2), ctypes.byref(vk2), 4096, 1)
+    base2 = lib.attn_chunk_bwd_workspace_size(ctypes.byref(vq2), ctypes.byref(vk2))
+    wsb_full = torch.empty(int(full2), dtype=torch.uint8, device=dev)
+    wsb_base = torch.empty(int(base2), dtype=torch.uint8, device=dev)
+    g2 = (torch.empty_like(q2), torch.empty_like(k2), torch.empty_like(v2))
+    tb_split = timed(lambda: lsx.chunked_bwd(q2, k2, v2, o2, l2, do2, 4096, True, dq=g2[0],
+                                             dk=g2[1], dv=g2[2], workspace=wsb_full))
+    tb_whole = timed(lambda: lsx.chunked_bwd(q2, k2, v2, o2, l2, do2, 4096, True, dq=g2[0],
+                                             dk=g2[1], dv=g2[2], workspace=wsb_base))
+    _, fb2 = flops(1, 1, n2, 128, True)
+    out["split_cols_bwd_16k_h1"] = {
+        "split": full2 > base2,
+        "ms_split": round(tb_split, 3), "ms_unsplit": round(tb_whole, 3),
+        "speedup": round(tb_whole / tb_split, 3),
+        "tflops_split": round(fb2 / (tb_split / 1e3) / 1e12, 1),
+        "workload": "B=1 H=1 N=16384 d=128 causal, backward (chunked_bwd)"}
+    del q2, k2, v2, do2, o2, l2, g2, wsb_full, wsb_base
     torch.cuda.empty_cache()
     return out
 

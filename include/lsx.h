@@ -269,8 +269,18 @@ int attn_chunk_bwd_noalloc(const lsx_tensor* q, const lsx_tensor* k,
  * those partials (for the current device's SM count); a workspace only as
  * large as attn_chunk_fwd_workspace_size, or none, runs the unsplit launch.
  * Otherwise the forward workspace holds the key-contiguous copy of V (as
- * attn_chunk_fwd) and the backward workspace what attn_chunk_bwd uses; the
- * backward never splits.
+ * attn_chunk_fwd).
+ *
+ * Backward, split key columns: its work items are (batch, kv head, key
+ * tile), each walking the query tiles that see the key tile for every head
+ * of the group.  When those items number fewer than the SMs (bf16, D = 64
+ * or 128, not in deterministic mode), each item's steps are cut into pieces
+ * (about four pieces of work per SM, at most 32 per item); every piece adds
+ * its dQ contributions as usual and writes partial fp32 dK, dV to the
+ * workspace, which one more kernel sums per key row (the result equals the
+ * unsplit one up to fp32 rounding of the sums).
+ * attn_chunked_bwd_workspace_size counts those partials; a workspace only as
+ * large as attn_chunk_bwd_workspace_size runs the unsplit launch.
  * ---------------------------------------------------------------------- */
 size_t attn_chunked_fwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal);

@@ -65,6 +65,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "bwd_split.h"
 #include "internal.h"
 #include "ptx.cuh"
 #include "tma_host.h"
@@ -112,6 +113,12 @@ struct BwdParams {
   int acc_tma;
   uint64_t* trace;  // per-CTA schedule record (NULL: not traced)
   int trace_kid;
+  // fused dK/dV with key columns split into pieces of piece_w steps (the
+  // dkdv kernel's kSplit form): piece i of every item writes its partial
+  // dK, dV (fp32) to slot i of part_dk / part_dv [kmax][B][Hkv][Lk][D]
+  int64_t piece_w, kmax;
+  float* part_dk;
+  float* part_dv;
 };
 
 // Row pitch (elements) of the transposed fp32 dQ accumulator [.][128][Np]:
@@ -332,8 +339,25 @@ struct DkdvItem {
   int64_t len;  // query tiles per head of the group
 };
 
-__device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
+// The piece of a split item (kept apart from DkdvItem, which the unsplit
+// kernel keeps in registers).
+struct DkdvPiece {
+  int64_t s0 = 0;     // first step of the piece
+  int64_t piece = 0;  // slot of its partials
+  bool empty = false; // past the item's last step: skipped by every role
+};
+
+template <bool kSplit>
+__device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it,
+                                              DkdvPiece* pc = nullptr) {
   DkdvItem x;
+  if constexpr (kSplit) {
+    // piece-major: every item's first piece (longest first), then every
+    // item's second, ...
+    const int64_t per_piece = p.n_ktiles * p.B * p.Hkv;
+    pc->piece = it / per_piece;
+    it -= pc->piece * per_piece;
+  }
   int64_t rank, bh;
   banded_item(it, p.n_ktiles, p.B * p.Hkv, &rank, &bh);
   x.j = rank;  // key tile 0 (the most query tiles) first
@@ -343,6 +367,12 @@ __device__ __forceinline__ DkdvItem dkdv_item(const BwdParams& p, int64_t it) {
   x.i0 = q_tile_begin(p, x.j);
   x.len = p.col_list == nullptr ? p.n_qtiles - x.i0 : p.col_count[x.j];
   x.n_i = x.len * x.group;  // (head, query tile) steps
+  if constexpr (kSplit) {
+    pc->s0 = pc->piece * p.piece_w;
+    pc->empty = pc->s0 >= x.n_i;
+    const int64_t n = x.n_i - pc->s0;
+    x.n_i = n < 0 ? 0 : (n > p.piece_w ? p.piece_w : n);
+  }
   return x;
 }
 
@@ -355,6 +385,10 @@ struct DkdvCursor {
 };
 __device__ __forceinline__ DkdvCursor dkdv_first(const DkdvItem& x) {
   return DkdvCursor{x.hk * x.group, 0};
+}
+// ... and at step s0 (the first step of a piece: one division per item)
+__device__ __forceinline__ DkdvCursor dkdv_at(const DkdvItem& x, int64_t s0) {
+  return DkdvCursor{x.hk * x.group + s0 / x.len, s0 % x.len};
 }
 // Query head and query tile of the cursor's step, then on to the next step.
 __device__ __forceinline__ void dkdv_take(const BwdParams& p, const DkdvItem& x, DkdvCursor& cur,
@@ -416,7 +450,7 @@ __host__ __device__ constexpr uint64_t seq_b_step(int kk) {
 // -delta) to every score of each query column; the grad warps then need
 // neither the LSE nor delta.  Without kRS warp 0 gathers both into shared
 // memory and the grad warps apply them per element.
-template <int D, bool kRS, bool kDq>
+template <int D, bool kRS, bool kDq, bool kSplit = false>
 __global__ void __launch_bounds__(640, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q,
                 const __grid_constant__ CUtensorMap tm_k,
@@ -501,7 +535,9 @@ __global__ void __launch_bounds__(640, 1)
       for (;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
-        const DkdvItem x = dkdv_item(p, it);
+        DkdvPiece pc;
+        const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;  // (every role skips the same items)
         if (!mbar_wait(&sm.kv_empty, kv_phase ^ 1, guard)) break;
         kv_phase ^= 1;
         if (lane == 0) {
@@ -510,7 +546,7 @@ __global__ void __launch_bounds__(640, 1)
           load_tile<D, false>(sm.v, &tm_v, &sm.kv_full, x.j * 128, x.hk, x.b);
         }
         bool ok = true;
-        DkdvCursor cur = dkdv_first(x);
+        DkdvCursor cur = kSplit ? dkdv_at(x, pc.s0) : dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s) {
           int64_t h, i;
           dkdv_take(p, x, cur, h, i);
@@ -570,7 +606,9 @@ __global__ void __launch_bounds__(640, 1)
       for (int64_t r = 0; ones_ok; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
-        const DkdvItem x = dkdv_item(p, it);
+        DkdvPiece pc;
+        const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;  // (every role skips the same items)
         if (!mbar_wait(&sm.kv_full, kv_phase, guard)) break;
         kv_phase ^= 1;
         tc_fence_after();
@@ -704,7 +742,9 @@ __global__ void __launch_bounds__(640, 1)
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
-        const DkdvItem x = dkdv_item(p, it);
+        DkdvPiece pc;
+        const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;  // (every role skips the same items)
         if (!mbar_wait(&sm.kv_full, kv_phase, guard)) break;
         kv_phase ^= 1;
         bool ok = true;
@@ -774,9 +814,11 @@ __global__ void __launch_bounds__(640, 1)
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
-        const DkdvItem x = dkdv_item(p, it);
+        DkdvPiece pc;
+        const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;  // (every role skips the same items)
         bool ok = true;
-        DkdvCursor cur = dkdv_first(x);
+        DkdvCursor cur = kSplit ? dkdv_at(x, pc.s0) : dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s, ++m) {
           int64_t h, i;
           dkdv_take(p, x, cur, h, i);
@@ -804,9 +846,11 @@ __global__ void __launch_bounds__(640, 1)
       for (int64_t r = 0;; ++r) {
         const int64_t it = snake_item(c, r, G);
         if (it >= p.n_items) break;
-        const DkdvItem x = dkdv_item(p, it);
+        DkdvPiece pc;
+        const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+        if (kSplit && pc.empty) continue;  // (every role skips the same items)
         bool ok = true;
-        DkdvCursor cur = dkdv_first(x);
+        DkdvCursor cur = kSplit ? dkdv_at(x, pc.s0) : dkdv_first(x);
         for (int64_t s = 0; s < x.n_i; ++s) {
           int64_t h, i;
           dkdv_take(p, x, cur, h, i);
@@ -908,10 +952,12 @@ __global__ void __launch_bounds__(640, 1)
     for (int64_t r = 0;; ++r) {
       const int64_t it = snake_item(c, r, G);
       if (it >= p.n_items) break;
-      const DkdvItem x = dkdv_item(p, it);
+      DkdvPiece pc;
+      const DkdvItem x = dkdv_item<kSplit>(p, it, &pc);
+      if (kSplit && pc.empty) continue;  // (every role skips the same items)
       const int64_t key_abs = p.kv_off + x.j * 128 + row;
       bool ok = true;
-      DkdvCursor cur = dkdv_first(x);
+      DkdvCursor cur = kSplit ? dkdv_at(x, pc.s0) : dkdv_first(x);
       for (int64_t s = 0; s < x.n_i; ++s) {
         int64_t h, i;
         dkdv_take(p, x, cur, h, i);
@@ -1079,6 +1125,13 @@ __global__ void __launch_bounds__(640, 1)
           for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
         if (!valid) continue;
+        if constexpr (kSplit) {
+          // this piece's partial rows, fp32, into its slot
+          const int64_t prow = ((pc.piece * p.B + x.b) * p.Hkv + x.hk) * p.Lk + krow;
+          store_row32(qtr < 2 ? p.part_dv : p.part_dk, 1, prow * D + col0 + cc * 32, u,
+                      qtr < 2 ? 1.f : p.scale, 0);
+          continue;
+        }
         if (qtr < 2)
           store_row32(p.dv, p.dv_f32,
                       x.b * p.dv_sb + x.hk * p.dv_sh + krow * p.dv_sn + col0 + cc * 32, u, 1.f,
@@ -1497,13 +1550,57 @@ bool map_ones(CUtensorMap* m, void* ones) {
   return make_map_bf16_rows8(m, ones, 1, 1, 256);
 }
 
+// The pieces of split key columns (BwdSplit): one warp per key row of dK
+// and dV, lane l owning columns [l E, l E + E).  A row has as many pieces as
+// its item has: ceil(steps / piece_w), steps = the query tiles that see its
+// key tile times the heads of the group (from the same causal geometry the
+// kernel used); pieces are summed in the order 0, 1, ...
+template <int D>
+__global__ void __launch_bounds__(256) dkdv_sum_pieces_kernel(const BwdParams p) {
+  constexpr int E = D / 32;
+  const int lane = threadIdx.x & 31;
+  const int64_t rows = p.B * p.Hkv * p.Lk;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  for (int64_t row = w0; row < rows; row += nw) {
+    const int64_t n = row % p.Lk, bh = row / p.Lk;
+    const int64_t b = bh / p.Hkv, hk = bh % p.Hkv;
+    const int64_t steps = (p.n_qtiles - q_tile_begin(p, n / 128)) * (p.Hq / p.Hkv);
+    const int64_t parts = (steps + p.piece_w - 1) / p.piece_w;
+    float ak[E], av[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) ak[e] = av[e] = 0.f;
+    for (int64_t q = 0; q < parts; ++q) {
+      const int64_t off = (q * rows + row) * D + lane * E;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        ak[e] += __ldcs(p.part_dk + off + e);
+        av[e] += __ldcs(p.part_dv + off + e);
+      }
+    }
+    const int64_t ok = b * p.dk_sb + hk * p.dk_sh + n * p.dk_sn + lane * E;
+    const int64_t ov = b * p.dv_sb + hk * p.dv_sh + n * p.dv_sn + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      if (p.dk_f32)
+        static_cast<float*>(p.dk)[ok + e] = ak[e];
+      else
+        static_cast<__nv_bfloat16*>(p.dk)[ok + e] = __float2bfloat16_rn(ak[e]);
+      if (p.dv_f32)
+        static_cast<float*>(p.dv)[ov + e] = av[e];
+      else
+        static_cast<__nv_bfloat16*>(p.dv)[ov + e] = __float2bfloat16_rn(av[e]);
+    }
+  }
+}
+
 template <int D>
 int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                     const lsx_tensor& lse, const lsx_tensor& d_o, const float* delta,
                     const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
                     float scale, const lsx_tensor& dq, const lsx_tensor& dk,
                     const lsx_tensor& dv, int accumulate, const DeviceCtx& ctx,
-                    cudaStream_t s, const BlockLists* bl) {
+                    cudaStream_t s, const BlockLists* bl, const BwdSplit* split) {
   // fused dK/dV/dQ: D = 128, not in deterministic mode, and somewhere to
   // add dQ into (the fp32 accumulator in the workspace, or an f32 dq)
   const bool fused = !ctx.deterministic && (cp.dq_acc != nullptr || dq.dtype == LSX_F32);
@@ -1555,9 +1652,22 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
   p.acc_sb = p.acc_sh = p.acc_sn = 0;
   p.trace = nullptr;
   p.trace_kid = 0;
+  p.piece_w = 0;
+  p.kmax = 1;
+  p.part_dk = p.part_dv = nullptr;
+  const bool split_on = split != nullptr && split->piece_w > 0;
+  if (split_on) {
+    // the fused form with the statistics on the tensor cores only
+    if (!fused || !rs || bl != nullptr || accumulate || split->kmax < 1)
+      return LSX_ERR_UNSUPPORTED;
+    p.piece_w = split->piece_w;
+    p.kmax = split->kmax;
+    p.part_dk = split->part_dk;
+    p.part_dv = split->part_dv;
+  }
 
-  // dK, dV (and dQ): items (key tile, b, kv head)
-  p.n_items = p.n_ktiles * q.B * k.H;
+  // dK, dV (and dQ): items (key tile, b, kv head), times the pieces if split
+  p.n_items = p.n_ktiles * q.B * k.H * p.kmax;
   CUtensorMap tacc = tk;  // (unused unless p.acc_tma)
   p.acc_tma = 0;
   if (fused) {
@@ -1592,7 +1702,8 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
                                           p.acc_sn))
       p.acc_tma = 1;
     const size_t smem = sizeof(DkdvSmem<D>) + 1024;
-    auto kern = rs ? dkdv_kernel<D, true, true> : dkdv_kernel<D, false, true>;
+    auto kern = split_on ? dkdv_kernel<D, true, true, true>
+                         : (rs ? dkdv_kernel<D, true, true> : dkdv_kernel<D, false, true>);
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return LSX_ERR_LAUNCH;
@@ -1603,6 +1714,15 @@ int launch_bwd_tc_d(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& 
     kern<<<static_cast<unsigned>(grid), 640, smem, s>>>(tq, tk, tv, tdo, trs, tones, tacc, p);
     timing_end(kKidBwdFused, s);
     if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
+    if (split_on) {
+      const int64_t rows = k.B * k.H * k.N;
+      int64_t blocks = (rows * 32 + 255) / 256;
+      if (blocks > 8 * ctx.sm_count) blocks = 8 * ctx.sm_count;
+      timing_begin(kKidTreeMerge, s);
+      dkdv_sum_pieces_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, s>>>(p);
+      timing_end(kKidTreeMerge, s);
+      if (cudaGetLastError() != cudaSuccess) return LSX_ERR_LAUNCH;
+    }
     if (direct) return LSX_OK;
     if (D == 128) {
       timing_begin(kKidDqConvert, s);
@@ -1700,10 +1820,26 @@ int launch_bwd_tc(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
                   cudaStream_t s, const BlockLists* bl) {
   if (q.D == 128)
     return launch_bwd_tc_d<128>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
-                                dk, dv, accumulate, ctx, s, bl);
+                                dk, dv, accumulate, ctx, s, bl, nullptr);
   if (q.D == 64)
     return launch_bwd_tc_d<64>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
-                               dk, dv, accumulate, ctx, s, bl);
+                               dk, dv, accumulate, ctx, s, bl, nullptr);
+  return LSX_ERR_UNSUPPORTED;
+}
+
+int launch_bwd_tc_split(const lsx_tensor& q, const lsx_tensor& k, const lsx_tensor& v,
+                        const lsx_tensor& lse, const lsx_tensor& d_o, const float* delta,
+                        const BwdCopies& cp, int64_t q_off, int64_t kv_off, int causal,
+                        float scale, const lsx_tensor& dq, const lsx_tensor& dk,
+                        const lsx_tensor& dv, const BwdSplit& split, const DeviceCtx& ctx,
+                        cudaStream_t s) {
+  if (split.piece_w <= 0) return LSX_ERR_UNSUPPORTED;
+  if (q.D == 128)
+    return launch_bwd_tc_d<128>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
+                                dk, dv, 0, ctx, s, nullptr, &split);
+  if (q.D == 64)
+    return launch_bwd_tc_d<64>(q, k, v, lse, d_o, delta, cp, q_off, kv_off, causal, scale, dq,
+                               dk, dv, 0, ctx, s, nullptr, &split);
   return LSX_ERR_UNSUPPORTED;
 }
 

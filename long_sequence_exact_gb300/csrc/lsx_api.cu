@@ -11,6 +11,7 @@
 #include <mutex>
 #include <vector>
 
+#include "bwd_split.h"
 #include "fwd_split.h"
 #include "internal.h"
 #include "ptx.cuh"
@@ -343,13 +344,15 @@ size_t attn_chunk_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k) {
   return n;
 }
 
-int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
-                   const lsx_tensor* v, const lsx_tensor* o,
-                   const lsx_tensor* lse, const lsx_tensor* d_o,
-                   int64_t q_off, int64_t kv_off, int causal, float scale,
-                   const lsx_tensor* dq, const lsx_tensor* dk,
-                   const lsx_tensor* dv, int accumulate, void* workspace,
-                   size_t workspace_bytes, lsx_stream_t stream) {
+// attn_chunk_bwd, and attn_chunked_bwd's split form (split != NULL: the
+// full workspace's copies are required and its partials follow them)
+static int chunk_bwd_impl(const lsx_tensor* q, const lsx_tensor* k,
+                          const lsx_tensor* v, const lsx_tensor* o,
+                          const lsx_tensor* lse, const lsx_tensor* d_o,
+                          int64_t q_off, int64_t kv_off, int causal, float scale,
+                          const lsx_tensor* dq, const lsx_tensor* dk,
+                          const lsx_tensor* dv, int accumulate, void* workspace,
+                          size_t workspace_bytes, lsx_stream_t stream, const BwdSplit* split) {
   LSX_TRY(check_qkv(q, k, v));
   LSX_TRY(check_view(o));
   LSX_TRY(check_view(d_o));
@@ -396,8 +399,24 @@ int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
   if (q->dtype == LSX_F32)
     return launch_simt_bwd(*q, *k, *v, *lse, *d_o, delta, q_off, kv_off,
                            causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
+  if (split != nullptr) {
+    if (copies.stats.rows == nullptr || accumulate) return LSX_ERR_WORKSPACE;
+    return launch_bwd_tc_split(*q, *k, *v, *lse, *d_o, delta, copies, q_off, kv_off,
+                               causal != 0, sc, *dq, *dk, *dv, *split, ctx, s);
+  }
   return launch_bwd_tc(*q, *k, *v, *lse, *d_o, delta, copies, q_off, kv_off,
                        causal != 0, sc, *dq, *dk, *dv, accumulate != 0, ctx, s);
+}
+
+int attn_chunk_bwd(const lsx_tensor* q, const lsx_tensor* k,
+                   const lsx_tensor* v, const lsx_tensor* o,
+                   const lsx_tensor* lse, const lsx_tensor* d_o,
+                   int64_t q_off, int64_t kv_off, int causal, float scale,
+                   const lsx_tensor* dq, const lsx_tensor* dk,
+                   const lsx_tensor* dv, int accumulate, void* workspace,
+                   size_t workspace_bytes, lsx_stream_t stream) {
+  return chunk_bwd_impl(q, k, v, o, lse, d_o, q_off, kv_off, causal, scale, dq, dk, dv,
+                        accumulate, workspace, workspace_bytes, stream, nullptr);
 }
 
 // ------------------------------------------- whole-sequence chunked calls
@@ -498,10 +517,58 @@ int attn_chunked_fwd(const lsx_tensor* q, const lsx_tensor* k,
                         workspace_bytes, stream);
 }
 
+// The backward's counterpart of plan_split: its items are (b, kv head, key
+// tile), each walking the query tiles that see the key tile for every head
+// of the group.  With fewer items than SMs those steps are cut into pieces
+// (about four pieces of work per SM, at most 32 per item); each piece
+// writes partial dK, dV that a sum kernel adds up.  Not in deterministic
+// mode (the partial sums would be one more reduction order to pin).
+static bool plan_split_bwd(const lsx_tensor& q, const lsx_tensor& k, int causal,
+                           const DeviceCtx& ctx, BwdSplit* out) {
+  if (ctx.deterministic || ctx.sm_count <= 0) return false;
+  if (q.dtype != LSX_BF16 || q.N <= 0 || k.N <= 0 || (q.D != 64 && q.D != 128)) return false;
+  const int64_t n_kt = ceil_div(k.N, 128), n_qt = ceil_div(q.N, 128);
+  if (k.B * k.H * n_kt >= static_cast<int64_t>(ctx.sm_count)) return false;
+  const int64_t group = q.H / k.H;
+  int64_t total = 0, longest = 0;
+  for (int64_t j = 0; j < n_kt; ++j) {
+    // query tiles that see key tile j (offsets 0, as in the chunked call)
+    int64_t i0 = 0;
+    if (causal) {
+      const int64_t need = 128 * j;
+      i0 = need > q.N - 1 ? n_qt : need / 128;
+    }
+    const int64_t steps = (n_qt - i0) * group;
+    total += steps;
+    if (steps > longest) longest = steps;
+  }
+  total *= k.B * k.H;
+  int64_t w = ceil_div(total, 4 * static_cast<int64_t>(ctx.sm_count));
+  if (w < 4) w = 4;
+  if (ceil_div(longest, w) > 32) w = ceil_div(longest, 32);
+  const int64_t kmax = ceil_div(longest, w);
+  if (kmax < 2) return false;
+  out->piece_w = w;
+  out->kmax = kmax;
+  return true;
+}
+
+static size_t split_bwd_bytes(const lsx_tensor& k, const BwdSplit& sp, size_t* one) {
+  *one = (static_cast<size_t>(sp.kmax) * k.B * k.H * k.N * k.D * sizeof(float) + 255) / 256 * 256;
+  return 2 * *one;
+}
+
 size_t attn_chunked_bwd_workspace_size(const lsx_tensor* q, const lsx_tensor* k,
                                        int64_t chunk_len, int causal) {
-  (void)chunk_len; (void)causal;
-  return attn_chunk_bwd_workspace_size(q, k);
+  (void)chunk_len;
+  const size_t base = attn_chunk_bwd_workspace_size(q, k);
+  if (base == 0 || q == nullptr || k == nullptr || q->dtype != LSX_BF16) return base;
+  DeviceCtx ctx;
+  if (device_ctx(&ctx) != LSX_OK) return base;
+  BwdSplit sp;
+  if (!plan_split_bwd(*q, *k, causal, ctx, &sp)) return base;
+  size_t one;
+  return base + split_bwd_bytes(*k, sp, &one);
 }
 
 int attn_chunked_bwd(const lsx_tensor* q, const lsx_tensor* k,
@@ -514,6 +581,21 @@ int attn_chunked_bwd(const lsx_tensor* q, const lsx_tensor* k,
   LSX_TRY(check_qkv(q, k, v));
   if (q->N != k->N) return LSX_ERR_SHAPE;
   if (chunk_len <= 0 || chunk_len % 128 != 0) return LSX_ERR_UNSUPPORTED;
+  // key columns split into pieces when the workspace holds their partials
+  // (see plan_split_bwd); otherwise one persistent launch
+  BwdSplit sp;
+  DeviceCtx ctx;
+  LSX_TRY(device_ctx(&ctx));
+  const size_t base = attn_chunk_bwd_workspace_size(q, k);
+  size_t one = 0;
+  if (workspace != nullptr && q->dtype == LSX_BF16 && plan_split_bwd(*q, *k, causal, ctx, &sp) &&
+      workspace_bytes >= base + split_bwd_bytes(*k, sp, &one)) {
+    char* ws = static_cast<char*>(workspace);
+    sp.part_dk = reinterpret_cast<float*>(ws + base);
+    sp.part_dv = reinterpret_cast<float*>(ws + base + one);
+    return chunk_bwd_impl(q, k, v, o, lse, d_o, 0, 0, causal, scale, dq, dk, dv, 0, workspace,
+                          base, stream, &sp);
+  }
   return attn_chunk_bwd(q, k, v, o, lse, d_o, 0, 0, causal, scale, dq, dk, dv, 0,
                         workspace, workspace_bytes, stream);
 }
