@@ -81,14 +81,18 @@ def test_full_mask_equals_dense_chunked_path():
     # its unsplit launch: these 48 query pairs would otherwise be split into
     # key pieces and merged, which rounds differently)
     vq, vk = _lib.view(q), _lib.view(k)
-    base = _lib.load().attn_chunk_fwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk))
+    lib = _lib.load()
+    base = lib.attn_chunk_fwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk))
     ws = torch.empty(base, dtype=torch.uint8, device=DEV)
+    # (likewise the backward: its 48 key-tile items would be split)
+    base_b = lib.attn_chunk_bwd_workspace_size(ctypes.byref(vq), ctypes.byref(vk))
+    ws_b = torch.empty(base_b, dtype=torch.uint8, device=DEV)
     for causal in (True, False):
         o1, l1 = lsx.block_sparse_fwd(q, k, v, full, causal)
         o2, l2 = lsx.chunked_fwd(q, k, v, 512, causal, workspace=ws)
         assert torch.equal(o1, o2) and torch.equal(l1, l2)
         g1 = lsx.block_sparse_bwd(q, k, v, o1, l1, d_o, full, causal)
-        g2 = lsx.chunked_bwd(q, k, v, o2, l2, d_o, 512, causal)
+        g2 = lsx.chunked_bwd(q, k, v, o2, l2, d_o, 512, causal, workspace=ws_b)
         # dK, dV identical; dQ's fp32 partial sums land in a varying order
         assert rel_fro(f64(g1[0]), f64(g2[0])) <= 1e-3
         for a, b in zip(g1[1:], g2[1:]):
