@@ -33,6 +33,8 @@ CASES = [
     (1, 1, 1, 1000, 1000, 128, 0, 0, True),     # several items per CTA
     (1, 2, 2, 1, 4096, 128, 4095, 0, True),     # one query row
     (2, 8, 8, 512, 2048, 128, 1536, 0, True),   # a diagonal chunk pair
+    (2, 16, 4, 1900, 1900, 64, 0, 0, True),     # d=64: items per CTA > 1, odd tile count
+    (2, 32, 8, 1024, 1024, 64, 0, 128, True),   # d=64: pair 0's first tile sees no key
 ]
 
 
