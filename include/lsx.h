@@ -208,16 +208,16 @@ int attn_block_sparse_bwd(const lsx_tensor* q, const lsx_tensor* k, const lsx_te
 
 /* ------------------------------------------------------------------------
  * attn_chunk_bwd_noalloc -- attn_chunk_bwd for callers that cannot allocate
- * device memory when they call it (the paper has no counterpart; this is a
- * deployment convenience of the library).  Examples: an extension running
- * inside a host application that owns the device memory pool and offers no
- * way to request more, or a latency-critical loop that forbids allocation
- * after start-up.  Same tensors, semantics and results as attn_chunk_bwd,
- * but no workspace argument: the row dot products go to a fixed 16 MiB array
- * compiled into the library (attn_chunk_bwd_noalloc_max_bytes()), which every
- * GPU that loads the library holds until the process exits; when the
- * sequence-contiguous operand copies of attn_chunk_bwd also fit, they are
- * placed there too.
+ * device memory when they call it (none of the cited methods has a
+ * counterpart; this is a deployment convenience of the library).  Examples:
+ * an extension running inside a host application that owns the device
+ * memory pool and offers no way to request more, or a latency-critical loop
+ * that forbids allocation after start-up.  Same tensors, semantics and
+ * results as attn_chunk_bwd, but no workspace argument: the row dot products
+ * go to a fixed 16 MiB array compiled into the library
+ * (attn_chunk_bwd_noalloc_max_bytes()), which every GPU that loads the
+ * library holds until the process exits; when the sequence-contiguous
+ * operand copies of attn_chunk_bwd also fit, they are placed there too.
  *  - Limit: attn_chunk_bwd_min_workspace_size(q, k) must not exceed that
  *    size (B * Hq * Lq <= 4,194,304 query rows); larger problems return
  *    LSX_ERR_WORKSPACE and launch nothing.
