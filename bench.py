@@ -81,23 +81,28 @@ def tile_pairs(b, h, n, causal=True):
     return b * h * (t * (t + 1) // 2 if causal else t * t)
 
 
-def recorded_traffic(name, units):
+def recorded_traffic(name, units, d, causal):
     """DRAM bytes per launch of kernel `name` scaled to `units` tile pairs,
-    from a committed ncu summary whose source hash matches the current
-    kernel source; None when there is none (never taken, or the kernel has
+    from a committed ncu summary of the same kernel source, head dimension
+    and masking (each head dimension is its own instantiation, with its own
+    traffic); None when there is none (never taken, or the kernel has
     changed since).  A profiles/*.md line reads
-      traffic: kernel=<name> source=<hash16> bytes=<dram read+write> units=<tile pairs>"""
+      traffic: kernel=<name> source=<hash16> d=<head dim> causal=<0|1>
+               bytes=<dram read+write> units=<tile pairs>
+    (on one line)."""
     import glob
-    import re
     want = kernel_source_hash(name)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         with open(path) as f:
             for line in f:
-                m = re.match(r"\s*traffic:\s*kernel=(\S+)\s+source=(\S+)\s+bytes=(\S+)\s+units=(\S+)",
-                             line)
-                if m and m.group(1) == name and m.group(2) == want:
-                    return {"bytes": float(m.group(3)) / float(m.group(4)) * units,
-                            "source": os.path.relpath(path, ROOT), "captured_units": float(m.group(4))}
+                if not line.lstrip().startswith("traffic:"):
+                    continue
+                kv = dict(t.split("=", 1) for t in line.split()[1:] if "=" in t)
+                if (kv.get("kernel") == name and kv.get("source") == want
+                        and kv.get("d") == str(d) and kv.get("causal") == str(int(causal))
+                        and "bytes" in kv and "units" in kv):
+                    return {"bytes": float(kv["bytes"]) / float(kv["units"]) * units,
+                            "source": os.path.relpath(path, ROOT), "captured_units": float(kv["units"])}
     return None
 
 
@@ -421,12 +426,12 @@ def run_ours(args, rank, world, local_rank):
             ent["achieved_tflops"] = round(ach, 1)
             ent["frac_of_peak"] = round(ach / pk["bf16_sustained"], 4)
             ent["frac_of_burst_peak"] = round(ach / pk["bf16"], 4)
-            rec = recorded_traffic(name, units) if name in KERNEL_SOURCES else None
+            rec = recorded_traffic(name, units, w.D, w.causal) if name in KERNEL_SOURCES else None
             ent["dram_bytes_per_launch"] = round(rec["bytes"]) if rec else None
         kernels[name] = ent
     if dom is not None and dom[0] in algo:
         name, (cnt, tot) = dom
-        rec = recorded_traffic(name, units)
+        rec = recorded_traffic(name, units, w.D, w.causal)
         traffic = args.traffic if args.traffic is not None else (round(rec["bytes"]) if rec else None)
         ach = algo[name] / (tot / cnt / 1e3) / 1e12
         roofline = {"kernel": name, "bound": "tensor", "achieved": round(ach, 1),

@@ -61,13 +61,17 @@ def test_recorded_traffic_matches_only_the_current_source(tmp_path, monkeypatch)
     prof = tmp_path / "profiles"
     prof.mkdir()
     (prof / "a.md").write_text(
-        "text\ntraffic: kernel=bwd_fused_tc source=0000000000000000 bytes=9 units=1\n"
-        f"traffic: kernel=bwd_fused_tc source={h} bytes=1000 units=10\n")
+        "text\ntraffic: kernel=bwd_fused_tc source=0000000000000000 d=128 causal=1 bytes=9 units=1\n"
+        f"traffic: kernel=bwd_fused_tc source={h} d=64 causal=0 bytes=7 units=1\n"
+        f"traffic: kernel=bwd_fused_tc source={h} d=128 causal=1 bytes=1000 units=10\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    rec = bench.recorded_traffic("bwd_fused_tc", 25)
+    rec = bench.recorded_traffic("bwd_fused_tc", 25, 128, True)
     assert rec["bytes"] == pytest.approx(2500.0)  # 100 bytes per unit x 25 units
     assert rec["source"] == os.path.join("profiles", "a.md")
-    assert bench.recorded_traffic("fwd_tc", 25) is None
+    assert bench.recorded_traffic("bwd_fused_tc", 25, 64, False)["bytes"] == pytest.approx(175.0)
+    # another head dimension or masking is another kernel's traffic
+    assert bench.recorded_traffic("bwd_fused_tc", 25, 64, True) is None
+    assert bench.recorded_traffic("fwd_tc", 25, 128, True) is None
 
 
 def test_committed_traffic_record_is_well_formed():
@@ -79,5 +83,6 @@ def test_committed_traffic_record_is_well_formed():
             if line.startswith("traffic:"):
                 rec = dict(kv.split("=") for kv in line.split()[1:])
     assert rec is not None and rec["kernel"] == "bwd_fused_tc"
+    assert rec["d"] == "128" and rec["causal"] == "1"
     assert int(rec["units"]) == bench.tile_pairs(1, 16, 65536)
     assert len(rec["source"]) == 16 and int(rec["bytes"]) > 0
