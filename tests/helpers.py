@@ -89,7 +89,8 @@ BF16_U = 2.0 ** -8  # unit roundoff of bf16 (8 significant bits)
 ROUND_MULT = 4.0    # standard deviations of the rounding model a tile may reach
 
 
-def bf16_rounding_scales(q, k, v, d_o, o, lse, q_off=0, kv_off=0, causal=False, scale=None):
+def bf16_rounding_scales(q, k, v, d_o, o, lse, q_off=0, kv_off=0, causal=False, scale=None,
+                         block_mask=None):
     """Per-row standard deviations of the gradient error that the bf16
     roundings of the tensor-core backward produce, to first order, taking
     every rounding as an independent relative error of at most u = 2^-8:
@@ -104,14 +105,17 @@ def bf16_rounding_scales(q, k, v, d_o, o, lse, q_off=0, kv_off=0, causal=False, 
       dK_j: 2u scale sqrt(sum_r (dS_rj^2 + P_rj^2 a2_r) |q_r|^2)
       dV_j: u sqrt(sum_r P_rj^2 |dO_r|^2)
     (the sums over r run over the query rows of every head of j's group).
-    Arguments are float64 arrays as given to the oracle; o and lse are the
-    oracle's exact forward.  Returns ([B,Hq,Lq], [B,Hkv,Lk], [B,Hkv,Lk])."""
+    Arguments are float64 arrays as given to the oracle (block_mask as
+    well); o and lse are the oracle's exact forward.  Returns ([B,Hq,Lq],
+    [B,Hkv,Lk], [B,Hkv,Lk])."""
     from oracle import attention as A
     b, hq, lq, d = q.shape
     hkv, lk = k.shape[1], k.shape[2]
     scale = 1.0 / np.sqrt(d) if scale is None else scale
     c = 2.0 * BF16_U * scale
     vis = A.visible(q_off + np.arange(lq), kv_off + np.arange(lk), causal)
+    if block_mask is not None:
+        vis = vis & A.block_visible(np.arange(lq), np.arange(lk), block_mask)
     kn2, qn2, don2 = (k ** 2).sum(-1), (q ** 2).sum(-1), (d_o ** 2).sum(-1)
     sq = np.zeros((b, hq, lq))
     sk2 = np.zeros((b, hkv, lk))
