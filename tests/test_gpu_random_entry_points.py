@@ -164,3 +164,45 @@ def test_random_merges(i):
     o_ref, l_ref = A.tree_merge(f64(parts), f64(lses))
     check_lse(f64(l_), l_ref, lse_tol(l_ref))
     check_close(f64(o), o_ref, tol(o_ref))
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_fp32_chunk_pairs_merged(i):
+    """The fp32 path: a random chunk pair split at random key positions into
+    up to three key chunks, partials merged pairwise, gradients accumulated
+    over the key chunks from the merged O and LSE."""
+    r = np.random.default_rng(15000 + i)
+    d = int(r.choice([64, 128]))
+    hkv = int(r.integers(1, 3))
+    hq = hkv * int(r.choice([1, 2]))
+    b = int(r.integers(1, 3))
+    lq = int(r.integers(1, 300))
+    lk = int(r.integers(2, 400))
+    causal = bool(r.integers(0, 4) > 0)
+    q_off, kv_off = int(r.integers(0, 300)), int(r.integers(0, 300))
+    cuts = [0] + sorted(int(c) for c in r.choice(np.arange(1, lk), size=min(2, lk - 1),
+                                                  replace=False)) + [lk]
+    seed = 160 + 7 * i
+    f32 = torch.float32
+    q = random_tensor((b, hq, lq, d), seed, dtype=f32, device=DEV)
+    k = random_tensor((b, hkv, lk, d), seed + 1, dtype=f32, device=DEV)
+    v = random_tensor((b, hkv, lk, d), seed + 2, dtype=f32, device=DEV)
+    d_o = random_tensor((b, hq, lq, d), seed + 3, dtype=f32, device=DEV)
+    acc = None
+    for a, e in zip(cuts[:-1], cuts[1:]):
+        part = lsx.chunk_fwd(q, k[:, :, a:e], v[:, :, a:e], q_off, kv_off + a, causal)
+        acc = part if acc is None else lsx.merge(*acc, *part)
+    o, lse = acc
+    dq, dk, dv = torch.zeros_like(q), torch.zeros_like(k), torch.zeros_like(v)
+    for a, e in zip(cuts[:-1], cuts[1:]):
+        lsx.chunk_bwd(q, k[:, :, a:e], v[:, :, a:e], o, lse, d_o, q_off, kv_off + a, causal,
+                      dq=dq, dk=dk[:, :, a:e], dv=dv[:, :, a:e], accumulate=True)
+    torch.cuda.synchronize()
+    assert lsx.sync_status() == 0
+    Q, K, V, DO = f64(q), f64(k), f64(v), f64(d_o)
+    o_ref, lse_ref = A.attn_fwd(Q, K, V, q_off, kv_off, causal)
+    check_lse(f64(lse), lse_ref, TOL_FP32)
+    check_close(f64(o), o_ref, TOL_FP32)
+    for name, g, rr in zip(("dQ", "dK", "dV"), (dq, dk, dv),
+                           A.attn_bwd(Q, K, V, DO, q_off, kv_off, causal)):
+        check_close(f64(g), rr, TOL_FP32, name)
