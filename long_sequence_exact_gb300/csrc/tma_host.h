@@ -8,10 +8,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 namespace lsx {
 
+// The driver's encoder, looked up on first use (again after a failed look-up)
+// and cached; callers on several threads may get here at the same time.
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> cached{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
@@ -19,6 +24,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
                                          cudaEnableDefault, &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+      cached.store(fn, std::memory_order_release);
     }
   }
   return fn;
