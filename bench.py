@@ -273,6 +273,9 @@ def run_ours(args, rank, world, local_rank):
         w = w.with_(N=args.n or w.N, Hq=args.heads or w.Hq, Hkv=args.heads or w.Hkv)
         workload = (f"{w.name}_n{w.N}_h{w.Hq}_profiling" if args.workload
                     else f"causal_{w.N}_h{w.Hq}_profiling")
+    if args.deterministic:
+        lsx.set_deterministic(True)  # (before the workspace sizes: no split in this mode)
+        workload += "_deterministic"
     x = make_inputs(w, device=dev, seed=w.seed + rank)
     q, k, v, d_o = x["q"], x["k"], x["v"], x["d_o"]
     o = torch.empty_like(q)
@@ -467,6 +470,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1)*0.5 q/k/v, N(0,1) dO; one problem per rank)",
         "config": {"workload": workload, "B": w.B, "H": w.Hq, "N": w.N, "d": w.D,
                    "chunk_len": w.chunk, "causal": w.causal,
+                   "deterministic_backward": bool(args.deterministic),
                    "flops_per_step": step_flops, "fwd_flops": f_fwd, "bwd_flops": f_bwd,
                    "l2": (f"inputs larger than L2 (q, k, v, dO {in_bytes / 2**30:.3g} GiB each; "
                           "no flush needed)" if 4 * in_bytes > L2_BYTES else
@@ -862,6 +866,9 @@ def main():
     ap.add_argument("--workload", default=None,
                     choices=("causal_32k_ring", "causal_128k_balanced", "noncausal_64k_heavytail"),
                     help="another attention workload in place of the headline one (profiling)")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="the bit-repeatable backward (dK/dV kernel + owner-computes dQ kernel) "
+                         "in place of the fused one (profiling)")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
