@@ -157,9 +157,12 @@ __global__ void __launch_bounds__(256) merge_kernel(
 // over 16-byte pieces, four per thread per iteration, each piece combined
 // with its row's two LSE values.  A thread writes only the pieces it read,
 // so the output O may be one of the inputs.
+// D4: 16-byte pieces per row (D / 4), a constant so that the row of a piece
+// is a shift.
+template <int D4>
 __global__ void __launch_bounds__(256) merge_dense_kernel(
     const float4* __restrict__ oa, const float* __restrict__ la, const float4* __restrict__ ob,
-    const float* __restrict__ lb, float4* oo, float* lo, int64_t n4, int d4) {
+    const float* __restrict__ lb, float4* oo, float* lo, int64_t n4) {
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i0 < n4;
        i0 += 4 * stride) {
@@ -169,7 +172,7 @@ __global__ void __launch_bounds__(256) merge_dense_kernel(
     for (int u = 0; u < 4; ++u) {
       const int64_t i = i0 + u * stride;
       if (i < n4) {
-        const int64_t row = i / d4;
+        const int64_t row = i / D4;
         xa[u] = __ldcs(oa + i);
         xb[u] = __ldcs(ob + i);
         sa[u] = __ldg(la + row);
@@ -192,7 +195,7 @@ __global__ void __launch_bounds__(256) merge_dense_kernel(
           l = m + logf(tot);
         }
         __stcs(oo + i, r);
-        if (i % d4 == 0) lo[i / d4] = l;
+        if (i % D4 == 0) lo[i / D4] = l;
       }
     }
   }
@@ -501,17 +504,17 @@ int launch_merge(const lsx_tensor& oa, const lsx_tensor& la,
                      lo.data != la.data && lo.data != lb.data;
   if (dense) {
     const int64_t n4 = rows * oa.D / 4;
+    auto kern = oa.D == 128 ? merge_dense_kernel<32> : merge_dense_kernel<16>;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, merge_dense_kernel, 256, 0) !=
-            cudaSuccess || per_sm < 1)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, 0) != cudaSuccess ||
+        per_sm < 1)
       per_sm = 1;
     const int64_t need = ceil_div(n4, 256 * 4);
     const int64_t cap = static_cast<int64_t>(ctx.sm_count) * per_sm;
-    merge_dense_kernel<<<static_cast<int>(need < cap ? need : cap), 256, 0, s>>>(
+    kern<<<static_cast<int>(need < cap ? need : cap), 256, 0, s>>>(
         static_cast<const float4*>(oa.data), static_cast<const float*>(la.data),
         static_cast<const float4*>(ob.data), static_cast<const float*>(lb.data),
-        static_cast<float4*>(oo.data), static_cast<float*>(lo.data), n4,
-        static_cast<int>(oa.D / 4));
+        static_cast<float4*>(oo.data), static_cast<float*>(lo.data), n4);
     timing_end(kKidMerge, s);
     return cudaGetLastError() == cudaSuccess ? LSX_OK : LSX_ERR_LAUNCH;
   }
