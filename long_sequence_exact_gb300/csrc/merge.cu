@@ -98,6 +98,18 @@ struct RowIdx {
   int64_t H, N;
   __device__ __forceinline__ void split(int64_t row, int64_t& b, int64_t& h,
                                         int64_t& n) const {
+    if (row < (int64_t{1} << 31) && N < (int64_t{1} << 31) && H < (int64_t{1} << 31)) {
+      // 32-bit divisions where everything fits (a 64-bit one costs several
+      // times as many instructions, per row of every merge)
+      const uint32_t r = static_cast<uint32_t>(row), nn = static_cast<uint32_t>(N),
+                     hh = static_cast<uint32_t>(H);
+      const uint32_t bh = r / nn;
+      n = r - bh * nn;
+      const uint32_t bb = bh / hh;
+      h = bh - bb * hh;
+      b = bb;
+      return;
+    }
     n = row % N;
     const int64_t bh = row / N;
     h = bh % H;
