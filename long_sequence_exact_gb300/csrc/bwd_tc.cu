@@ -1508,29 +1508,34 @@ __global__ void __launch_bounds__(256) dq_convert_t_kernel(const float* __restri
     tile[d][lane] = (q0 + lane < Lq) ? src[d * np + q0 + lane] : 0.f;
   __syncthreads();
   const int64_t b = bh / Hq, h = bh % Hq;
+  // lane l writes dimensions (2l, 2l+1) and (64+2l, 65+2l) of each query:
+  // the tile reads of a warp then fall on 16 distinct banks twice (a
+  // two-way conflict), where four consecutive dimensions per lane gave four
+  // reads of four ways each
   for (int qq = w; qq < 32; qq += 8) {
     const int64_t q = q0 + qq;
     if (q >= Lq) break;
-    float4 a = make_float4(tile[4 * lane][qq], tile[4 * lane + 1][qq], tile[4 * lane + 2][qq],
-                           tile[4 * lane + 3][qq]);
-    const int64_t off = b * sb + h * sh + q * sn + 4 * lane;
-    if (f32) {
-      float4* d = reinterpret_cast<float4*>(static_cast<float*>(dq) + off);
-      if (accumulate) {
-        const float4 o = *d;
-        a.x += o.x; a.y += o.y; a.z += o.z; a.w += o.w;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int d0 = 64 * half + 2 * lane;
+      float2 a = make_float2(tile[d0][qq], tile[d0 + 1][qq]);
+      const int64_t off = b * sb + h * sh + q * sn + d0;
+      if (f32) {
+        float2* d = reinterpret_cast<float2*>(static_cast<float*>(dq) + off);
+        if (accumulate) {
+          const float2 o = *d;
+          a.x += o.x; a.y += o.y;
+        }
+        *d = a;
+      } else {
+        uint32_t* d = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(dq) + off);
+        if (accumulate) {
+          const uint32_t o = *d;
+          const __nv_bfloat162 pr = *reinterpret_cast<const __nv_bfloat162*>(&o);
+          a.x += __low2float(pr); a.y += __high2float(pr);
+        }
+        *d = pack_bf16(a.x, a.y);
       }
-      *d = a;
-    } else {
-      uint2* d = reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(dq) + off);
-      if (accumulate) {
-        const uint2 o = *d;
-        const __nv_bfloat162 lo = *reinterpret_cast<const __nv_bfloat162*>(&o.x);
-        const __nv_bfloat162 hi = *reinterpret_cast<const __nv_bfloat162*>(&o.y);
-        a.x += __low2float(lo); a.y += __high2float(lo);
-        a.z += __low2float(hi); a.w += __high2float(hi);
-      }
-      *d = make_uint2(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w));
     }
   }
 }
